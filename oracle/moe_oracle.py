@@ -1,0 +1,309 @@
+"""Plain fp64 CPU oracle of one Mixture-of-Experts FFN layer (forward pass).
+
+TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and bench.py's CPU
+baseline may use this module; the CUDA path never does. It is deliberately
+slow and literal: every stage follows the definition on the source pages, in
+float64, with numpy's matmul as the only library primitive and no blocking,
+fusion or reordering beyond what the definition states.
+
+Source pages (cited by the short names used below):
+  [ST]  shubhamtatvamasi.com/llm-inference/moe, "Mixture of Experts"
+  [KG]  klaylearn.com/glossary/mixture-of-experts, "Mixture of Experts" (glossary)
+  [KL]  klaylearn.com/inference-engineering/l/mixture-of-experts, lesson 06.05
+  [TB]  techbonafide.com, "Mixture of Experts (MoE) explained: why AI models
+        don't use every parameter at once"
+  [SA]  shipai.vats.cc/learn/advanced-concepts/mixture-of-experts, "Mixture of
+        Experts (MoE)"
+
+What the layer computes (the plainest reading of the pages):
+  1. logits l[t,e] = x[t] . W_r[e] (+ b[e])          [ST "The router"; Q&A "How does a top-k router work?"]
+  2. scores s = softmax over all E experts, or sigmoid per expert
+                                                     [ST "The router"; SA "How routing works"]
+  3. keep the k highest scores per token, ties to the lower expert index
+                                                     [ST "The router"; TB "How Does Routing Work"]
+  4. gates g_j = s_j / sum of the selected s (renormalised to sum to one)
+                                                     [ST "The router" and its Q&A]
+  5. group the (token, expert) pairs by destination expert; with a capacity
+     factor cf each expert keeps at most ceil(cf * T * k / E) tokens and the
+     overflow skips that expert ("continues on the residual path")
+                                                     [KG definition; ST "Load imbalance"; ST Q&A on capacity factor]
+  6. each kept pair runs its expert's MLP; the MLP form is not fixed by the
+     pages ("a standard feedforward block", TB "Experts as Specialized
+     Subnetworks"); this layer uses SwiGLU without biases:
+        y = W_down (silu(W_gate x) * (W_up x)),  silu(z) = z / (1 + exp(-z))
+  7. out[t] = sum over the token's kept slots j of g_j * y_j, plus every shared
+     expert's MLP of x[t] with weight one           [ST "The router" (shared experts); KG definition]
+The residual add is outside the layer: a token whose every routed pair was
+dropped gets only its shared-expert part (zero when there is none).
+
+Readings where the pages are silent (each the plainest one):
+  * tie-break of equal scores: the lower expert index wins; slot order is the
+    rank order (highest score first);
+  * softmax is taken over all E logits before selection, then the selected
+    scores are renormalised (for softmax this equals a softmax over the
+    selected logits);
+  * which tokens overflow a full expert: tokens are admitted in ascending
+    token index, so the highest-index tokens are dropped;
+  * the capacity factor is the binary32 number the caller passes; the
+    ceiling is taken of its exact rational value times T*k/E;
+  * dropped pairs are not compensated: the remaining gates are not
+    renormalised again;
+  * a router bias, when present, is added to the logits before the score
+    function, so it moves both the selection and the gates.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from fractions import Fraction
+from typing import Callable, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "router_logits", "scores_from_logits", "select_topk", "gates_from_scores", "route",
+    "capacity", "dispatch", "silu", "expert_mlp", "combine", "layer_forward", "LayerResult",
+    "flops_per_pair", "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
+]
+
+
+# ---------------------------------------------------------------------------
+# 1-4: routing
+
+def router_logits(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray]) -> np.ndarray:
+    """l = x W_r^T (+ b): one logit per expert from one small linear layer [ST "The router"]."""
+    l = np.asarray(x, dtype=np.float64) @ np.asarray(w_router, dtype=np.float64).T
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float64)[None, :]
+    return l
+
+
+def scores_from_logits(logits: np.ndarray, score: str) -> np.ndarray:
+    """Softmax over all experts (max-subtracted), or the sigmoid variant [ST "The router"]."""
+    l = np.asarray(logits, dtype=np.float64)
+    if score == "softmax":
+        z = np.exp(l - l.max(axis=1, keepdims=True))
+        return z / z.sum(axis=1, keepdims=True)
+    if score == "sigmoid":
+        with np.errstate(over="ignore"):
+            return 1.0 / (1.0 + np.exp(-l))
+    raise ValueError(score)
+
+
+def select_topk(scores: np.ndarray, k: int):
+    """The k highest scores per token, in rank order; equal scores go to the lower index.
+
+    A stable sort of -s keeps equal scores in ascending expert order.
+    Returns (idx [T,k] int32, selected scores [T,k] float64).
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    order = np.argsort(-s, axis=1, kind="stable")[:, :k]
+    return order.astype(np.int32), np.take_along_axis(s, order, axis=1)
+
+
+def gates_from_scores(s_sel: np.ndarray, renormalize: bool = True) -> np.ndarray:
+    """Selected gate values renormalised to sum to one [ST "The router"; Q&A top-k router]."""
+    if not renormalize:
+        return np.array(s_sel, dtype=np.float64)
+    return s_sel / s_sel.sum(axis=1, keepdims=True)
+
+
+def route(x, w_router, bias, k: int, score: str, renormalize: bool = True):
+    """Stages 1-4. Returns (idx [T,k] int32, gate [T,k] f64, scores [T,E] f64)."""
+    s = scores_from_logits(router_logits(x, w_router, bias), score)
+    idx, s_sel = select_topk(s, k)
+    return idx, gates_from_scores(s_sel, renormalize), s
+
+
+# ---------------------------------------------------------------------------
+# 5: capacity and the permutation by destination expert
+
+def capacity(T: int, k: int, E: int, capacity_factor: float) -> Optional[int]:
+    """Per-expert limit ceil(cf * T*k/E) on the exact value of binary32 cf; None = dropless.
+
+    [ST "Load imbalance": at most capacity factor x ideal tokens; ST Q&A on
+    capacity factor: "factor x (T.k/E)".]
+    """
+    cf = float(np.float32(capacity_factor))
+    if cf <= 0.0:
+        return None
+    return math.ceil(Fraction(cf) * T * k / E)
+
+
+@dataclass
+class Dispatch:
+    counts: np.ndarray     # [E]   pairs routed to each expert, before capacity
+    kept: np.ndarray       # [E]   pairs each expert keeps
+    offsets: np.ndarray    # [E+1] exclusive scan of kept; offsets[E] = kept pairs P'
+    dest_row: np.ndarray   # [T,k] row of pair (t,j) in the grouped buffer, -1 if dropped
+    src_token: np.ndarray  # [P']  token of each grouped row
+
+
+def dispatch(idx: np.ndarray, n_experts: int, cap: Optional[int]) -> Dispatch:
+    """Group the (token, slot) pairs by expert, admitting tokens in ascending index.
+
+    "Permuting tokens by destination expert" [KG definition]; overflow beyond
+    the capacity skips the expert [ST "Load imbalance"].
+    """
+    T, k = idx.shape
+    per_expert: list[list[tuple[int, int]]] = [[] for _ in range(n_experts)]
+    seen = np.zeros(n_experts, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if cap is None or seen[e] < cap:
+                per_expert[e].append((t, j))
+            seen[e] += 1
+    counts = seen.astype(np.int32)
+    kept = np.array([len(p) for p in per_expert], dtype=np.int32)
+    offsets = np.zeros(n_experts + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(kept)
+    dest_row = np.full((T, k), -1, dtype=np.int32)
+    src_token = np.zeros(int(offsets[-1]), dtype=np.int32)
+    for e in range(n_experts):
+        for r, (t, j) in enumerate(per_expert[e]):
+            dest_row[t, j] = offsets[e] + r
+            src_token[offsets[e] + r] = t
+    return Dispatch(counts, kept, offsets, dest_row, src_token)
+
+
+# ---------------------------------------------------------------------------
+# 6: the expert MLP
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z))."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def expert_mlp(xrows: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray) -> np.ndarray:
+    """SwiGLU MLP of each row: W_down (silu(W_gate x) * (W_up x)).
+
+    xrows [n,d]; w_gate, w_up [F,d]; w_down [d,F]; returns [n,d] float64.
+    """
+    xr = np.asarray(xrows, dtype=np.float64)
+    g = xr @ np.asarray(w_gate, dtype=np.float64).T
+    u = xr @ np.asarray(w_up, dtype=np.float64).T
+    return (silu(g) * u) @ np.asarray(w_down, dtype=np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# 7: combine
+
+def combine(dest_row: np.ndarray, gate: np.ndarray, y_rows: np.ndarray,
+            shared: Optional[np.ndarray], d_model: int) -> np.ndarray:
+    """out[t] = sum over kept slots of gate * expert output, plus the shared part.
+
+    [ST Q&A "How does a top-k router work?": gate-weighted sum; ST "The router":
+    shared experts every token always visits.] Dropped slots add nothing.
+    """
+    T, k = dest_row.shape
+    out = np.zeros((T, d_model), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            r = int(dest_row[t, j])
+            if r >= 0:
+                out[t] += gate[t, j] * y_rows[r]
+    if shared is not None:
+        out += shared
+    return out
+
+
+# ---------------------------------------------------------------------------
+# whole layer
+
+@dataclass
+class LayerResult:
+    idx: np.ndarray
+    gate: np.ndarray
+    scores: np.ndarray
+    disp: Dispatch
+    cap: Optional[int]
+    tokens: np.ndarray          # the token ids whose outputs are in `out`
+    out: np.ndarray             # [len(tokens), d] float64
+
+
+ExpertFn = Callable[[int], Sequence[np.ndarray]]
+
+
+def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray], experts: ExpertFn,
+                  *, top_k: int, score: str = "softmax", renormalize: bool = True,
+                  capacity_factor: float = 0.0, n_shared: int = 0,
+                  tokens: Optional[np.ndarray] = None,
+                  routing: Optional[tuple] = None) -> LayerResult:
+    """The MoE FFN layer for all tokens, or only the outputs of `tokens`.
+
+    x [T,d] and w_router [E,d] are float64 (exact copies of the stored
+    values). experts(g) returns expert g's (W_gate [F,d], W_up [F,d],
+    W_down [d,F]) in float64; g = E .. E+S-1 are the shared experts. Routing
+    and capacity always cover all T tokens (admission depends on the whole
+    batch); only the MLP and combine are restricted to `tokens`.
+    `routing` = (idx, gate) replaces stages 1-4 (scores then come back None).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape
+    E = w_router.shape[0]
+    if routing is None:
+        idx, gate, s = route(x, w_router, bias, top_k, score, renormalize)
+    else:
+        idx, gate = routing
+        idx = np.asarray(idx, dtype=np.int32)
+        gate = np.asarray(gate, dtype=np.float64)
+        s = None
+    cap = capacity(T, top_k, E, capacity_factor)
+    disp = dispatch(idx, E, cap)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    want = np.zeros(T, dtype=bool)
+    want[tok] = True
+
+    y_rows = np.zeros((int(disp.offsets[-1]), d), dtype=np.float64)
+    for e in range(E):
+        rows = np.arange(disp.offsets[e], disp.offsets[e + 1])
+        rows = rows[want[disp.src_token[rows]]]
+        if rows.size == 0:
+            continue
+        wg, wu, wd = experts(e)
+        y_rows[rows] = expert_mlp(x[disp.src_token[rows]], wg, wu, wd)
+
+    shared = None
+    if n_shared > 0:
+        shared = np.zeros((T, d), dtype=np.float64)
+        for s_i in range(n_shared):
+            wg, wu, wd = experts(E + s_i)
+            shared[tok] += expert_mlp(x[tok], wg, wu, wd)
+    out = combine(disp.dest_row, gate, y_rows, shared, d)[tok]
+    return LayerResult(idx, gate, s, disp, cap, tok, out)
+
+
+# ---------------------------------------------------------------------------
+# accounting rules the pages state
+
+def flops_per_pair(d_model: int, d_ff: int) -> int:
+    """Multiply-adds of one SwiGLU expert on one token, counted as 2 flops each: 3 matrices of d x F."""
+    return 6 * d_model * d_ff
+
+
+def flops_per_token(active_params: float) -> float:
+    """FLOPs per token = 2 x active parameters [ST "Memory vs compute, quantified", table]."""
+    return 2.0 * active_params
+
+
+def weight_bytes(total_params: float, bytes_per_param: float) -> float:
+    """Resident weight memory = total parameters x bytes per parameter [ST same table]."""
+    return total_params * bytes_per_param
+
+
+def experts_touched_expected(E: int, k: int, batch: int) -> float:
+    """Expected experts read per step under uniform routing: E (1 - (1 - k/E)^batch).
+
+    [ST "Memory vs compute, quantified": the touched fraction is about
+    1 - (1 - k/E)^batch.] Exact for tokens that each pick a uniformly random
+    k-subset independently: each expert is missed by one token with
+    probability 1 - k/E.
+    """
+    return E * (1.0 - (1.0 - k / E) ** batch)
+
+
+def experts_touched(idx: np.ndarray, E: int) -> int:
+    """Number of distinct experts a routing reads."""
+    return int(np.unique(np.asarray(idx).ravel()).size) if np.asarray(idx).size else 0
