@@ -1,0 +1,219 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) Mixture-of-Experts FFN layer forward.
+ *
+ * One MoE layer, one GPU: router logits -> softmax or sigmoid scores -> top-k
+ * with renormalised gates -> grouping of tokens by destination expert
+ * (histogram, prefix sum, scatter; dropless or capacity-limited) -> grouped
+ * SwiGLU expert MLPs (plus an optional always-on shared expert) -> gate-weighted
+ * combine back in token order. Every stage is a CUDA kernel of libmoe.so.
+ *
+ * Source pages the operations follow (cited by these short names below):
+ *   [ST] shubhamtatvamasi.com/llm-inference/moe, "Mixture of Experts"
+ *   [KG] klaylearn.com/glossary/mixture-of-experts, "Mixture of Experts"
+ *   [TB] techbonafide.com, "Mixture of Experts (MoE) explained"
+ *   [SA] shipai.vats.cc/learn/advanced-concepts/mixture-of-experts, "Mixture of Experts (MoE)"
+ *
+ * Conventions shared by every call:
+ *   - All tensors are row-major and contiguous. Pointers marked "device" are
+ *     device memory the CALLER allocated and owns; the library never allocates,
+ *     frees or synchronises (except moe_get_device_error, which synchronises
+ *     the stream it is given).
+ *   - Device pointers to activations and weights must be 16-byte aligned; the
+ *     workspace must be 256-byte aligned.
+ *   - Element type of x, weights, x_perm, y_perm and out is cfg->dtype
+ *     (MOE_BF16 or MOE_F32); router scores, gates and the bias are float32;
+ *     indices are int32. bf16 paths accumulate in float32.
+ *   - Calls are asynchronous on `stream`. Arguments are validated on the host
+ *     first; a bad argument returns an error before anything is enqueued.
+ *     A failed launch returns MOE_ERR_CUDA. Problems found on the device
+ *     (an expert index out of range, offsets that are not a valid grouping, a
+ *     bounded wait that ran out) are recorded in the workspace status word
+ *     and read with moe_get_device_error. Nothing aborts or traps.
+ *   - G = n_experts + n_shared groups. Weight tensors hold the routed experts
+ *     first and the shared expert (if any) last:
+ *       w_gate, w_up : [G, d_ff, d_model]     w_down : [G, d_model, d_ff]
+ *   - R = moe_rows_capacity(cfg) = min(T*k, E*cap) rows hold the kept
+ *     (token, expert) pairs grouped by expert; the shared expert's T rows
+ *     follow at rows R .. R+T-1 of the grouped outputs.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, non-positive size, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle (see moe_config_t) */
+  MOE_ERR_WORKSPACE = 3,     /* ws_bytes < moe_workspace_size(cfg) */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel ran out */
+  MOE_ERR_DEVICE_INDEX = 6   /* device: an index or offset out of range was seen and skipped */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_score_t;
+
+/*
+ * Layer shape and policy.
+ *   T               tokens in the batch (1 .. 1048576)
+ *   d_model         hidden size d;   bf16: multiple of 128;  f32: multiple of 4
+ *   n_experts       routed experts E (1 .. 256)
+ *   top_k           experts per token k (1 .. min(E, 8))
+ *   d_ff            expert hidden size F;  bf16: multiple of 128;  f32: multiple of 4
+ *   n_shared        always-on shared experts S (0 or 1), same d_ff as the routed ones [ST "The router"]
+ *   score           MOE_SOFTMAX over all E logits, or MOE_SIGMOID per expert [ST "The router"]
+ *   renormalize     1: gates = selected scores / their sum [ST "The router"]; 0: gates = raw scores
+ *   capacity_factor <= 0: dropless; > 0: each expert keeps at most
+ *                   cap = ceil(capacity_factor * T * k / E) tokens, evaluated exactly on this binary32
+ *                   value, admitting tokens in ascending token index; the overflow pairs contribute
+ *                   nothing ("skips that expert and continues on the residual path", [ST "Load imbalance"])
+ *   dtype           MOE_BF16 or MOE_F32 (activations and weights)
+ */
+typedef struct moe_config {
+  int32_t T;
+  int32_t d_model;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t d_ff;
+  int32_t n_shared;
+  int32_t score;          /* moe_score_t */
+  int32_t renormalize;
+  float capacity_factor;
+  int32_t dtype;          /* moe_dtype_t */
+} moe_config_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(moe_status_t status);
+
+/* Host-side validation of a configuration: MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_check_config(const moe_config_t* cfg);
+
+/* Per-expert capacity cap (T when dropless); -1 for an invalid configuration. */
+int32_t moe_capacity(const moe_config_t* cfg);
+
+/* R = min(T*k, E*cap): rows of x_perm and src_token. -1 for an invalid configuration. */
+int64_t moe_rows_capacity(const moe_config_t* cfg);
+
+/* R + S*T: rows of y_perm (the shared expert's rows follow the routed ones). -1 if invalid. */
+int64_t moe_grouped_rows(const moe_config_t* cfg);
+
+/* Bytes of device workspace every call below needs (0 for an invalid configuration). */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Zero the workspace status word (asynchronous). Call once after allocating a workspace. */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Router: logits = x W_r^T (+ bias), scores, top-k, gates.
+ * [ST "The router" and Q&A "How does a top-k router work?"; SA "How routing works (intuition)"]
+ *   x         device [T, d_model]             w_router device [E, d_model]
+ *   bias      device [E] float32 or NULL; added to the logits before the score function
+ *   topk_idx  device [T, k] int32 out: expert ids in rank order (highest score first, equal
+ *             scores to the lower id); always k distinct ids in [0, E)
+ *   topk_gate device [T, k] float32 out: gates (sum to one when renormalize)
+ *   scores    device [T, E] float32 out, or NULL: the full softmax / sigmoid scores
+ */
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router,
+                             const float* bias, int32_t* topk_idx, float* topk_gate, float* scores,
+                             cudaStream_t stream);
+
+/*
+ * Grouping by destination expert [KG "Mixture of Experts" definition: permute tokens by
+ * destination expert; ST "Load imbalance": capacity limit or dropless].
+ *   topk_idx  device [T, k] int32 in (ids outside [0, E) are skipped and flagged)
+ *   x         device [T, d_model] in
+ *   counts    device [E] int32 out: pairs routed to each expert, before capacity
+ *   offsets   device [E+1] int32 out: exclusive scan of the kept counts; offsets[E] = P' kept pairs
+ *   dest_row  device [T, k] int32 out: row of pair (t, j) in x_perm, or -1 when dropped
+ *   src_token device [R] int32 out: token of each grouped row (rows >= P' untouched)
+ *   x_perm    device [R, d_model] out: x[src_token[r]] for r < P' (rows >= P' untouched)
+ * Rows of one expert are in ascending token order, so the result is deterministic.
+ */
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const void* x,
+                         int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_token,
+                         void* x_perm, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Grouped expert MLPs [KG definition: "grouped GEMMs on each expert's batch"; TB "Experts as
+ * Specialized Subnetworks"]: for every routed expert e and kept row r in
+ * [offsets[e], offsets[e+1]) and, for the shared expert, every token t:
+ *     y = W_down (silu(W_gate a) * (W_up a)),  silu(z) = z * sigmoid(z)
+ * with a = x_perm[r] (routed) or x[t] (shared). bf16: the intermediate silu(.)*(.) is
+ * rounded to bf16 once before the down projection, y is rounded to bf16 from the
+ * float32 accumulator.
+ *   x_perm  device [R, d_model] in        offsets device [E+1] int32 in (validated on the device)
+ *   x       device [T, d_model] in (read only when n_shared > 0; may be NULL otherwise)
+ *   w_gate, w_up device [G, d_ff, d_model]; w_down device [G, d_model, d_ff]
+ *   y_perm  device [R + S*T, d_model] out: routed rows r < P', then the shared rows R + t
+ */
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                             const void* x, const void* w_gate, const void* w_up, const void* w_down,
+                             void* y_perm, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Combine [ST Q&A "How does a top-k router work?": gate-weighted sum of the selected experts;
+ * ST "The router": shared experts every token visits; KG definition: undo the permutation]:
+ *     out[t] = sum_{j: dest_row[t,j] >= 0} gate[t,j] * y_perm[dest_row[t,j]]  (+ y_perm[R + t] if S = 1)
+ * accumulated in float32 in slot order, shared part last. No residual add.
+ *   y_perm device [R + S*T, d_model] in; dest_row device [T, k] int32; topk_gate device [T, k] float32
+ *   out    device [T, d_model] out
+ */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* dest_row,
+                         const float* topk_gate, void* out, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/*
+ * The whole layer: router -> permute -> grouped MLPs -> combine, enqueued on `stream`
+ * with no host synchronisation (capturable in a CUDA graph).
+ *   out            device [T, d_model] out: the MoE FFN output (no residual add)
+ *   topk_idx_out   device [T, k] int32 out or NULL (routing is then kept in the workspace)
+ *   counts_out     device [E] int32 out or NULL (per-expert load before capacity)
+ */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router,
+                               const float* bias, const void* w_gate, const void* w_up,
+                               const void* w_down, void* out, int32_t* topk_idx_out,
+                               int32_t* counts_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_layer_forward that also records CUDA events between its stages, for timing:
+ * events[0] before the router, [1] after the router, [2] after the grouping (histogram,
+ * scan, scatter, row gather), [3] after the gate/up GEMM, [4] after the down GEMM,
+ * [5] after the combine. `events` holds n_events cudaEvent_t handles (n_events <= 6;
+ * the first n_events boundaries are recorded).
+ */
+moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                     const float* bias, const void* w_gate, const void* w_up,
+                                     const void* w_down, void* out, int32_t* topk_idx_out,
+                                     int32_t* counts_out, void* ws, size_t ws_bytes,
+                                     void* const* events, int32_t n_events, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then return the first device-side status recorded in the workspace
+ * since the last moe_workspace_init / moe_clear_device_error (MOE_OK if none).
+ */
+moe_status_t moe_get_device_error(const void* ws, cudaStream_t stream);
+
+/* Reset the workspace status word to MOE_OK (asynchronous). */
+moe_status_t moe_clear_device_error(void* ws, cudaStream_t stream);
+
+/*
+ * Self-test of the bounded wait used by the pipelined kernels: one CTA waits on an
+ * mbarrier that nothing completes, gives up after about `limit_ns` nanoseconds, records
+ * MOE_ERR_TIMEOUT in the workspace status word and returns normally. Lets a caller check,
+ * without hanging the GPU, that a stalled pipeline surfaces as a status.
+ */
+moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns,
+                                       cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

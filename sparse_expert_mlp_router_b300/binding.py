@@ -1,0 +1,205 @@
+"""ctypes binding of libmoe.so: same names as the C ABI (include/moe.h), argument marshalling only.
+
+Tensors are torch tensors on the GPU; every call passes their data pointers and
+the current CUDA stream to the library, checks the returned status and raises
+MoeError on failure. No computation happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from .build import LIB_PATH
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
+    MOE_ERR_DEVICE_INDEX = range(7)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SOFTMAX, MOE_SIGMOID = 0, 1
+
+# Every symbol include/moe.h declares.
+EXPORTS = [
+    "moe_status_string", "moe_check_config", "moe_capacity", "moe_rows_capacity", "moe_grouped_rows",
+    "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
+    "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
+    "moe_clear_device_error", "moe_selftest_bounded_wait",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+        ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_shared", ctypes.c_int32),
+        ("score", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
+        ("dtype", ctypes.c_int32),
+    ]
+
+    def __repr__(self):
+        return "MoeConfig(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+def make_config(T: int, d_model: int, n_experts: int, top_k: int, d_ff: int, n_shared: int = 0,
+                score: str = "softmax", renormalize: bool = True, capacity_factor: float = 0.0,
+                dtype: str = "bf16") -> MoeConfig:
+    return MoeConfig(T, d_model, n_experts, top_k, d_ff, n_shared,
+                     MOE_SOFTMAX if score == "softmax" else MOE_SIGMOID, 1 if renormalize else 0,
+                     float(capacity_factor), MOE_BF16 if dtype == "bf16" else MOE_F32)
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_cfgp = ctypes.POINTER(MoeConfig)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe.so. Raises if the library has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run `python -m sparse_expert_mlp_router_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, i64, sz, u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
+        sig = {
+            "moe_status_string": ([i32], ctypes.c_char_p),
+            "moe_check_config": ([_cfgp], i32),
+            "moe_capacity": ([_cfgp], i32),
+            "moe_rows_capacity": ([_cfgp], i64),
+            "moe_grouped_rows": ([_cfgp], i64),
+            "moe_workspace_size": ([_cfgp], sz),
+            "moe_workspace_init": ([_vp, sz, _vp], i32),
+            "moe_router_topk": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
+            "moe_permute": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp], i32),
+            "moe_grouped_ffn": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp], i32),
+            "moe_combine": ([_cfgp, _vp, _vp, _vp, _vp, _vp, sz, _vp], i32),
+            "moe_layer_forward": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp], i32),
+            "moe_layer_forward_timed": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz,
+                                         ctypes.POINTER(_vp), i32, _vp], i32),
+            "moe_get_device_error": ([_vp, _vp], i32),
+            "moe_clear_device_error": ([_vp, _vp], i32),
+            "moe_selftest_bounded_wait": ([_vp, sz, u64, _vp], i32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str) -> None:
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+# ------------------------------------------------------------------ queries
+
+def moe_check_config(cfg: MoeConfig) -> int:
+    return lib().moe_check_config(ctypes.byref(cfg))
+
+
+def moe_capacity(cfg: MoeConfig) -> int:
+    return lib().moe_capacity(ctypes.byref(cfg))
+
+
+def moe_rows_capacity(cfg: MoeConfig) -> int:
+    return lib().moe_rows_capacity(ctypes.byref(cfg))
+
+
+def moe_grouped_rows(cfg: MoeConfig) -> int:
+    return lib().moe_grouped_rows(ctypes.byref(cfg))
+
+
+def moe_workspace_size(cfg: MoeConfig) -> int:
+    return lib().moe_workspace_size(ctypes.byref(cfg))
+
+
+# -------------------------------------------------------------- workspace
+
+def alloc_workspace(cfg: MoeConfig, device="cuda"):
+    """A zero-status workspace of moe_workspace_size(cfg) bytes (torch uint8 tensor)."""
+    import torch
+    n = moe_workspace_size(cfg)
+    if n == 0:
+        raise MoeError(moe_check_config(cfg) or MOE_ERR_INVALID_ARG, "moe_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_workspace_init(ws, stream=None) -> None:
+    _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+def moe_get_device_error(ws, stream=None) -> int:
+    return lib().moe_get_device_error(_ptr(ws), _stream(stream))
+
+
+def moe_clear_device_error(ws, stream=None) -> None:
+    _check(lib().moe_clear_device_error(_ptr(ws), _stream(stream)), "moe_clear_device_error")
+
+
+def moe_selftest_bounded_wait(ws, limit_ns: int, stream=None) -> None:
+    _check(lib().moe_selftest_bounded_wait(_ptr(ws), ws.numel(), int(limit_ns), _stream(stream)),
+           "moe_selftest_bounded_wait")
+
+
+# ------------------------------------------------------------------ stages
+
+def moe_router_topk(cfg, x, w_router, bias, topk_idx, topk_gate, scores=None, stream=None) -> None:
+    _check(lib().moe_router_topk(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
+                                 _ptr(topk_gate), _ptr(scores), _stream(stream)), "moe_router_topk")
+
+
+def moe_permute(cfg, topk_idx, x, counts, offsets, dest_row, src_token, x_perm, ws, stream=None) -> None:
+    _check(lib().moe_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
+                             _ptr(dest_row), _ptr(src_token), _ptr(x_perm), _ptr(ws), ws.numel(),
+                             _stream(stream)), "moe_permute")
+
+
+def moe_grouped_ffn(cfg, x_perm, offsets, x, w_gate, w_up, w_down, y_perm, ws, stream=None) -> None:
+    _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(x), _ptr(w_gate),
+                                 _ptr(w_up), _ptr(w_down), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_ffn")
+
+
+def moe_combine(cfg, y_perm, dest_row, topk_gate, out, ws, stream=None) -> None:
+    _check(lib().moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(dest_row), _ptr(topk_gate), _ptr(out),
+                             _ptr(ws), ws.numel(), _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, ws, topk_idx_out=None,
+                      counts_out=None, stream=None) -> None:
+    _check(lib().moe_layer_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate),
+                                   _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx_out), _ptr(counts_out),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_timed(cfg, x, w_router, bias, w_gate, w_up, w_down, out, ws, events,
+                            topk_idx_out=None, counts_out=None, stream=None) -> None:
+    """events: up to 6 torch.cuda.Event(enable_timing=True) recorded at the stage boundaries."""
+    handles = (_vp * len(events))(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_timed(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate),
+                                         _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx_out),
+                                         _ptr(counts_out), _ptr(ws), ws.numel(), handles, len(events),
+                                         _stream(stream)), "moe_layer_forward_timed")

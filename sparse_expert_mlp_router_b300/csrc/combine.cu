@@ -1,0 +1,138 @@
+// Gate-weighted combine back in token order, and the bounded-wait self-test.
+//
+// out[t] = sum over the token's kept slots j of gate[t,j] * y[dest_row[t,j]],
+// plus the shared expert's row with weight one. Follows
+// shubhamtatvamasi.com/llm-inference/moe "Mixture of Experts", Q&A "How does
+// a top-k router work?" (the output is the gate-weighted sum of the selected
+// experts' outputs) and section "The router" (shared experts every token
+// visits), and klaylearn.com/glossary/mixture-of-experts (undo the
+// permutation). A dropped slot (dest_row = -1) contributes nothing: the token
+// "continues on the residual path" for that expert (same page, "Load
+// imbalance"); the residual add itself is outside this layer.
+//
+// One CTA per token; each thread owns 16 bytes of the row and accumulates its
+// slots in float32 in slot order, the shared row last. All loads and stores are
+// coalesced 16-byte vectors.
+#include "internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+template <typename TE>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kN = 8;
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int kN = 4;
+  __device__ static void load(const float* p, float (&v)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+  __device__ static void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+
+template <typename TE>
+__global__ void combine_kernel(const TE* __restrict__ y, const int32_t* __restrict__ dest_row,
+                               const float* __restrict__ gate, TE* __restrict__ out, int d, int k, int S, int T,
+                               int64_t R, int32_t* status) {
+  constexpr int V = Vec<TE>::kN;
+  const int t = blockIdx.x;
+  __shared__ int32_t s_row[kMaxTopK];
+  __shared__ float s_gate[kMaxTopK];
+  if (threadIdx.x < k) {
+    int r = dest_row[(size_t)t * k + threadIdx.x];
+    if (r >= R) {
+      set_status(status, MOE_ERR_DEVICE_INDEX);
+      r = -1;
+    }
+    s_row[threadIdx.x] = r < 0 ? -1 : r;
+    s_gate[threadIdx.x] = gate[(size_t)t * k + threadIdx.x];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x * V; c < d; c += blockDim.x * V) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = s_row[j];
+      if (r < 0) continue;
+      float v[V];
+      Vec<TE>::load(y + (size_t)r * d + c, v);
+      const float g = s_gate[j];
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(g, v[i], acc[i]);
+    }
+    for (int s = 0; s < S; ++s) {
+      float v[V];
+      Vec<TE>::load(y + (size_t)(R + (int64_t)s * T + t) * d + c, v);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += v[i];
+    }
+    Vec<TE>::store(out + (size_t)t * d + c, acc);
+  }
+}
+
+// One CTA waits on an mbarrier that no one arrives on; the bounded wait gives up.
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, limit_ns))
+      set_status(status, MOE_ERR_TIMEOUT);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_row, const float* gate, void* out,
+                           int32_t* status, cudaStream_t st) {
+  const int V = (s.dtype == MOE_BF16) ? 8 : 4;
+  int threads = (s.d / V + 31) / 32 * 32;
+  if (threads > 256) threads = 256;
+  if (threads < 32) threads = 32;
+  if (s.dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<s.T, threads, 0, st>>>(static_cast<const __nv_bfloat16*>(y), dest_row, gate,
+                                                          static_cast<__nv_bfloat16*>(out), s.d, s.k, s.S, s.T, s.R,
+                                                          status);
+  else
+    combine_kernel<float><<<s.T, threads, 0, st>>>(static_cast<const float*>(y), dest_row, gate,
+                                                  static_cast<float*>(out), s.d, s.k, s.S, s.T, s.R, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

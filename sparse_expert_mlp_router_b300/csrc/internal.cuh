@@ -1,0 +1,114 @@
+// Internal declarations shared by the kernels of libmoe.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- limits ---
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kChunk = 128;          // tokens per chunk of the grouping kernels
+
+// ------------------------------------------------------ workspace layout ---
+// Byte offsets inside the caller's workspace; every segment is 256-byte aligned.
+struct WsLayout {
+  size_t status;        // int32 status word (+ padding)
+  size_t topk_idx;      // [T*k] int32
+  size_t topk_gate;     // [T*k] float
+  size_t chunk_counts;  // [nchunks*E] int32: per-chunk histogram, then per-chunk rank base
+  size_t counts;        // [E] int32
+  size_t offsets;       // [E+1] int32
+  size_t sched;         // [4*(G+1)] int32: group schedule of the grouped GEMMs
+  size_t dest_row;      // [T*k] int32
+  size_t src_token;     // [R] int32
+  size_t x_perm;        // [R*d] elements
+  size_t h;             // [(R+S*T)*F] elements: silu(gate) * up
+  size_t y;             // [(R+S*T)*d] elements: expert outputs
+  size_t total;
+};
+
+struct Shape {
+  int T, d, E, k, F, S, G;
+  int score, renorm, dtype;
+  int cap;            // per-expert capacity (T when dropless)
+  int64_t R;          // rows of the grouped buffer for routed pairs
+  int nchunks;
+  size_t esize;       // bytes per activation / weight element
+};
+
+Shape make_shape(const moe_config_t& c);
+WsLayout make_layout(const Shape& s);
+
+// Group schedule (device, int32), G groups:
+//   tile_start[G+1]  prefix sum of 128-row M tiles per group
+//   a_row[G]         first A row of the group (x_perm row, or x row 0 for the shared group)
+//   out_row[G]       first output row of the group in h / y
+//   rows[G]          rows of the group
+struct SchedView {
+  int32_t* tile_start;
+  int32_t* a_row;
+  int32_t* out_row;
+  int32_t* rows;
+};
+inline SchedView sched_view(void* base, int G) {
+  int32_t* p = static_cast<int32_t*>(base);
+  return SchedView{p, p + (G + 1), p + (G + 1) + G, p + (G + 1) + 2 * G};
+}
+
+// ------------------------------------------------------- device helpers ---
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float bf16_to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ------------------------------------------------------------- launchers ---
+// Each returns cudaGetLastError() after enqueueing.
+cudaError_t launch_router_fma(const Shape& s, const void* x, const void* w, const float* bias,
+                              int32_t* idx, float* gate, float* scores, cudaStream_t st);
+cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const float* bias,
+                             int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st);
+
+cudaError_t launch_group_hist(const Shape& s, const int32_t* idx, int32_t* chunk_counts,
+                              int32_t* status, cudaStream_t st);
+cudaError_t launch_group_scan(const Shape& s, int32_t* chunk_counts, int32_t* counts,
+                              int32_t* offsets, cudaStream_t st);
+cudaError_t launch_group_scatter(const Shape& s, const int32_t* idx, const int32_t* chunk_base,
+                                 const int32_t* offsets, int32_t* dest_row, int32_t* src_token,
+                                 cudaStream_t st);
+cudaError_t launch_gather_rows(const Shape& s, const void* x, const int32_t* src_token,
+                               const int32_t* offsets, void* x_perm, cudaStream_t st);
+
+cudaError_t launch_group_schedule(const Shape& s, const int32_t* offsets, void* sched,
+                                  int32_t* status, cudaStream_t st);
+cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
+                           const void* w_up, const void* w_down, const void* sched, void* h, void* y,
+                           cudaStream_t st);
+cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void* x,
+                                  const void* w_gate, const void* w_up, const void* sched, void* h,
+                                  int32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_down,
+                                const void* sched, void* y, int32_t* status, cudaStream_t st);
+
+cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_row,
+                           const float* gate, void* out, int32_t* status, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(int32_t* status, uint64_t limit_ns, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

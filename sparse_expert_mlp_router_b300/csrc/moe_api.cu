@@ -1,0 +1,352 @@
+// The C ABI of libmoe.so: host-side validation, workspace layout and the
+// enqueueing of the stage kernels. Declarations and their documentation are in
+// include/moe.h.
+#include <cmath>
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace moe {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Exact ceil(cf * T * k / E) on the binary32 value of cf, clamped to [1, T].
+// cf = m * 2^e with m a 24-bit integer; the quotient is evaluated in 128-bit integers.
+int exact_capacity(float cf, int T, int k, int E) {
+  if (!(cf > 0.0f)) return T;
+  int ex = 0;
+  const float fr = std::frexp(cf, &ex);                    // cf = fr * 2^ex, fr in [0.5, 1)
+  const unsigned __int128 m = (unsigned __int128)(uint64_t)std::ldexp(fr, 24);   // exact
+  const int e = ex - 24;
+  unsigned __int128 num = m * (unsigned __int128)T * (unsigned __int128)k;
+  unsigned __int128 den = (unsigned __int128)E;
+  if (e >= 0) {
+    if (e > 40) return T;
+    num <<= e;
+  } else {
+    if (-e > 100) return 1;
+    den <<= -e;
+  }
+  const unsigned __int128 q = (num + den - 1) / den;
+  if (q >= (unsigned __int128)T) return T;
+  return q < 1 ? 1 : (int)q;
+}
+
+moe_status_t check_cfg(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d_model < 1 || c->n_experts < 1 || c->top_k < 1 || c->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || (c->score != MOE_SOFTMAX && c->score != MOE_SIGMOID)) return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (std::isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->T > (1 << 20) || c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > 1)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_BF16) {
+    if (c->d_model % 128 != 0 || c->d_ff % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (c->d_model % 4 != 0 || c->d_ff % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)c->d_model * c->d_ff * (c->n_experts + c->n_shared) > (int64_t)1 << 40) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+Shape make_shape(const moe_config_t& c) {
+  Shape s{};
+  s.T = c.T;
+  s.d = c.d_model;
+  s.E = c.n_experts;
+  s.k = c.top_k;
+  s.F = c.d_ff;
+  s.S = c.n_shared;
+  s.G = s.E + s.S;
+  s.score = c.score;
+  s.renorm = c.renormalize;
+  s.dtype = c.dtype;
+  s.cap = exact_capacity(c.capacity_factor, s.T, s.k, s.E);
+  const int64_t tk = (int64_t)s.T * s.k, ec = (int64_t)s.E * s.cap;
+  s.R = tk < ec ? tk : ec;
+  s.nchunks = (s.T + kChunk - 1) / kChunk;
+  s.esize = (c.dtype == MOE_BF16) ? 2 : 4;
+  return s;
+}
+
+WsLayout make_layout(const Shape& s) {
+  WsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const size_t pairs = (size_t)s.T * s.k;
+  const size_t grouped = (size_t)s.R + (size_t)s.S * s.T;
+  L.status = take(kAlign);
+  L.topk_idx = take(pairs * 4);
+  L.topk_gate = take(pairs * 4);
+  L.chunk_counts = take((size_t)s.nchunks * s.E * 4);
+  L.counts = take((size_t)s.E * 4);
+  L.offsets = take((size_t)(s.E + 1) * 4);
+  L.sched = take((size_t)4 * (s.G + 1) * 4);
+  L.dest_row = take(pairs * 4);
+  L.src_token = take((size_t)s.R * 4);
+  L.x_perm = take((size_t)s.R * s.d * s.esize);
+  L.h = take(grouped * s.F * s.esize);
+  L.y = take(grouped * s.d * s.esize);
+  L.total = o;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t check_ws(const Shape& s, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// The stage bodies, shared by the stage entry points and the whole-layer call.
+cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
+                       float* gate, float* scores, int32_t* status, cudaStream_t st) {
+  (void)status;
+  return launch_router_fma(s, x, w_router, bias, idx, gate, scores, st);
+}
+
+cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx, const void* x,
+                        int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_token, void* x_perm,
+                        cudaStream_t st) {
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* cc = at<int32_t>(ws, L.chunk_counts);
+  cudaError_t e;
+  if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
+  if ((e = launch_group_scan(s, cc, counts, offsets, st)) != cudaSuccess) return e;
+  if ((e = launch_group_scatter(s, idx, cc, offsets, dest_row, src_token, st)) != cudaSuccess) return e;
+  return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
+}
+
+cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const int32_t* offsets,
+                    const void* x, const void* wg, const void* wu, const void* wd, void* y, cudaStream_t st,
+                    cudaEvent_t mid_event) {
+  int32_t* status = at<int32_t>(ws, L.status);
+  void* sched = at<void>(ws, L.sched);
+  void* h = at<void>(ws, L.h);
+  cudaError_t e;
+  if ((e = launch_group_schedule(s, offsets, sched, status, st)) != cudaSuccess) return e;
+  if (s.dtype == MOE_BF16) {
+    if ((e = launch_gemm_gateup_tc(s, x_perm, x, wg, wu, sched, h, status, st)) != cudaSuccess) return e;
+    if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+    return launch_gemm_down_tc(s, h, wd, sched, y, status, st);
+  }
+  if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+  return launch_ffn_fma(s, x_perm, x, wg, wu, wd, sched, h, y, st);
+}
+
+moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                           const void* w_gate, const void* w_up, const void* w_down, void* out,
+                           int32_t* topk_idx_out, int32_t* counts_out, void* ws, size_t ws_bytes,
+                           void* const* events, int n_events, cudaStream_t st) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
+      !aligned(w_down, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4)) ||
+      (topk_idx_out && !aligned(topk_idx_out, 4)) || (counts_out && !aligned(counts_out, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (n_events < 0 || n_events > 6 || (n_events > 0 && events == nullptr)) return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+  const WsLayout L = make_layout(s);
+  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  for (int i = 0; i < n_events; ++i) ev[i] = static_cast<cudaEvent_t>(events[i]);
+
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+  float* gate = at<float>(ws, L.topk_gate);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* dest_row = at<int32_t>(ws, L.dest_row);
+  int32_t* src_token = at<int32_t>(ws, L.src_token);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* y = at<void>(ws, L.y);
+
+  cudaError_t e = cudaSuccess;
+  if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((e = run_router(s, x, w_router, bias, idx, gate, nullptr, status, st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((e = run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, st)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev[2] && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((e = run_ffn(s, L, ws, x_perm, offsets, x, w_gate, w_up, w_down, y, st, ev[3])) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (ev[4] && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((e = launch_combine(s, y, dest_row, gate, out, status, st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ev[5] && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration outside what the kernels handle";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime or launch failure";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX: an out-of-range index or offset was skipped";
+  }
+  return "unknown moe_status_t";
+}
+
+moe_status_t moe_check_config(const moe_config_t* cfg) { return check_cfg(cfg); }
+
+int32_t moe_capacity(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return make_shape(*cfg).cap;
+}
+
+int64_t moe_rows_capacity(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return make_shape(*cfg).R;
+}
+
+int64_t moe_grouped_rows(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  const Shape s = make_shape(*cfg);
+  return s.R + (int64_t)s.S * s.T;
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return make_layout(make_shape(*cfg)).total;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 256, stream));
+}
+
+moe_status_t moe_clear_device_error(void* ws, cudaStream_t stream) {
+  if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(int32_t), stream));
+}
+
+moe_status_t moe_get_device_error(const void* ws, cudaStream_t stream) {
+  if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(v);
+}
+
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                             int32_t* topk_idx, float* topk_gate, float* scores, cudaStream_t stream) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!x || !w_router || !topk_idx || !topk_gate) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || (bias && !aligned(bias, 4)) || !aligned(topk_idx, 4) ||
+      !aligned(topk_gate, 4) || (scores && !aligned(scores, 4)))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  return cuda_status(run_router(s, x, w_router, bias, topk_idx, topk_gate, scores, nullptr, stream));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const void* x, int32_t* counts,
+                         int32_t* offsets, int32_t* dest_row, int32_t* src_token, void* x_perm, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!topk_idx || !x || !counts || !offsets || !dest_row || !src_token || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(x, 16) || !aligned(counts, 4) || !aligned(offsets, 4) ||
+      !aligned(dest_row, 4) || !aligned(src_token, 4) || !aligned(x_perm, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+  return cuda_status(run_permute(s, make_layout(s), ws, topk_idx, x, counts, offsets, dest_row, src_token, x_perm,
+                                 stream));
+}
+
+moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets, const void* x,
+                             const void* w_gate, const void* w_up, const void* w_down, void* y_perm, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && !x) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_perm, 16) || !aligned(offsets, 4) || (x && !aligned(x, 16)) || !aligned(w_gate, 16) ||
+      !aligned(w_up, 16) || !aligned(w_down, 16) || !aligned(y_perm, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+  return cuda_status(run_ffn(s, make_layout(s), ws, x_perm, offsets, x ? x : x_perm, w_gate, w_up, w_down, y_perm,
+                             stream, nullptr));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* dest_row,
+                         const float* topk_gate, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!y_perm || !dest_row || !topk_gate || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_perm, 16) || !aligned(dest_row, 4) || !aligned(topk_gate, 4) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+  return cuda_status(launch_combine(s, y_perm, dest_row, topk_gate, out, at<int32_t>(ws, make_layout(s).status),
+                                    stream));
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                               const void* w_gate, const void* w_up, const void* w_down, void* out,
+                               int32_t* topk_idx_out, int32_t* counts_out, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, topk_idx_out, counts_out, ws, ws_bytes,
+                       nullptr, 0, stream);
+}
+
+moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                     const float* bias, const void* w_gate, const void* w_up, const void* w_down,
+                                     void* out, int32_t* topk_idx_out, int32_t* counts_out, void* ws,
+                                     size_t ws_bytes, void* const* events, int32_t n_events, cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, topk_idx_out, counts_out, ws, ws_bytes,
+                       events, n_events, stream);
+}
+
+moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns, cudaStream_t stream) {
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+  if (limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_selftest(static_cast<int32_t*>(ws), limit_ns, stream));
+}
+
+}  // extern "C"

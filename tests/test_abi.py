@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: libmoe.so loads, exports what include/moe.h declares, and
+its host-side logic (validation, capacity, workspace sizing) behaves as documented.
+No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+import sparse_expert_mlp_router_b300 as moe
+from sparse_expert_mlp_router_b300.build import LIB_PATH
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    assert os.path.exists(LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    declared = _declared_symbols()
+    assert len(declared) >= 16
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(moe.EXPORTS)
+
+
+def _cfg(**kw):
+    base = dict(T=4096, d_model=7168, n_experts=256, top_k=8, d_ff=2048, n_shared=1, score="sigmoid",
+                capacity_factor=1.25, dtype="bf16")
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+def test_status_strings():
+    for code in range(7):
+        assert moe.status_string(code).startswith("MOE_")
+    assert "unknown" in moe.status_string(99)
+
+
+def test_config_validation():
+    assert moe.moe_check_config(_cfg()) == moe.MOE_OK
+    assert moe.moe_check_config(_cfg(top_k=9, n_experts=8)) == moe.MOE_ERR_INVALID_ARG   # k > E
+    assert moe.moe_check_config(_cfg(T=0)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_config(_cfg(d_model=100)) == moe.MOE_ERR_UNSUPPORTED          # bf16 needs d % 128
+    assert moe.moe_check_config(_cfg(d_model=100, d_ff=100, dtype="f32")) == moe.MOE_OK
+    assert moe.moe_check_config(_cfg(n_experts=512)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_config(_cfg(top_k=9, n_experts=16)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_config(_cfg(n_shared=2)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_config(_cfg(capacity_factor=float("nan"))) == moe.MOE_ERR_INVALID_ARG
+    assert moe.lib().moe_check_config(None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_workspace_size(_cfg(T=0)) == 0
+
+
+@pytest.mark.parametrize("T,k,E,cf", [
+    (4096, 8, 256, 1.25), (10, 1, 4, 1.0), (5, 1, 2, 0.8), (6, 1, 2, 0.5), (333, 8, 32, 1.1),
+    (257, 6, 48, 1.25), (1, 1, 1, 0.001), (100, 2, 8, 0.0), (100, 2, 8, -3.0), (7, 3, 5, 1e30),
+    (8192, 8, 128, 0.3), (999, 7, 13, 2.0 / 3.0),
+])
+def test_capacity_is_exact_ceiling(T, k, E, cf):
+    ref = O.capacity(T, k, E, cf)
+    ref = T if ref is None else min(ref, T)
+    c = moe.make_config(T=T, d_model=128, n_experts=E, top_k=k, d_ff=128, capacity_factor=cf)
+    assert moe.moe_capacity(c) == ref
+    assert moe.moe_rows_capacity(c) == min(T * k, E * ref)
+
+
+def test_workspace_grows_with_rows():
+    small = moe.moe_workspace_size(_cfg(capacity_factor=0.5))
+    big = moe.moe_workspace_size(_cfg(capacity_factor=0.0))
+    assert 0 < small < big
+    c = _cfg()
+    assert moe.moe_grouped_rows(c) == moe.moe_rows_capacity(c) + 4096
+    assert moe.moe_workspace_size(c) % 256 == 0
+
+
+def test_host_validation_rejects_before_any_launch():
+    c = _cfg()
+    L = moe.lib()
+    # null data pointers: rejected on the host, nothing is enqueued
+    assert L.moe_router_topk(ctypes.byref(c), None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_forward(ctypes.byref(c), None, None, None, None, None, None, None, None, None, None, 0,
+                               None) == moe.MOE_ERR_INVALID_ARG
+    # misaligned pointers
+    p = 0x10000
+    assert L.moe_router_topk(ctypes.byref(c), p + 2, p, None, p, p, None, None) == moe.MOE_ERR_INVALID_ARG
+    # workspace too small / misaligned
+    assert L.moe_permute(ctypes.byref(c), p, p, p, p, p, p, p, p, 256, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_permute(ctypes.byref(c), p, p, p, p, p, p, p, p + 16, 1 << 40, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(ctypes.byref(c), p, p, p, p, p, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_selftest_bounded_wait(None, 0, 10, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_init(p + 8, 4096, None) == moe.MOE_ERR_INVALID_ARG
+    # unsupported configuration reaches no launch either
+    bad = _cfg(d_model=100)
+    assert L.moe_grouped_ffn(ctypes.byref(bad), p, p, p, p, p, p, p, p, 1 << 40, None) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_timed_variant_rejects_bad_event_count():
+    c = _cfg()
+    p = 0x10000
+    L = moe.lib()
+    ev = (ctypes.c_void_p * 7)()
+    n = moe.moe_workspace_size(c)
+    assert L.moe_layer_forward_timed(ctypes.byref(c), p, p, None, p, p, p, p, None, None, p, n, ev, 7,
+                                     None) == moe.MOE_ERR_INVALID_ARG

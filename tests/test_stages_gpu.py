@@ -1,0 +1,138 @@
+"""Stage-by-stage parity of the C ABI against the fp64 oracle on the reduced workloads.
+
+Each stage is fed the GPU's own output of the stage before, so a mismatch
+points at exactly one kernel. Workloads span several GEMM tiles with ragged
+tails (T not a multiple of 128, uneven expert loads, empty experts, capacity
+drops, a shared expert, float32 and bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+import sparse_expert_mlp_router_b300 as moe
+from moe_cases import Inputs, assert_close, cfg_of, check_routing, out_tolerance, score_tolerance, to_f64
+
+pytestmark = pytest.mark.gpu
+
+MINI = synth.workloads.MINI
+
+
+def _router(w, inp, dev, cfg):
+    T, k, E = w.T, w.top_k, w.n_experts
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    gate = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    scores = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    moe.moe_router_topk(cfg, dev["x"], dev["w_router"], dev["bias"], idx, gate, scores)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), gate.cpu().numpy().astype(np.float64), scores.cpu().numpy().astype(np.float64), idx, gate
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_router_matches_oracle(name):
+    w = synth.WORKLOADS[name]
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    idx, gate, scores, _, _ = _router(w, inp, dev, cfg)
+    ref_scores = O.scores_from_logits(O.router_logits(inp.f64["x"], inp.f64["w_router"], inp.bias), w.score)
+    tol = score_tolerance(w)
+    assert np.abs(scores - ref_scores).max() <= tol
+    check_routing(idx, ref_scores, w.top_k)
+    ref_gate = O.gates_from_scores(np.take_along_axis(ref_scores, idx.astype(np.int64), axis=1), w.renormalize)
+    assert np.abs(gate - ref_gate).max() <= tol
+    if w.renormalize:
+        assert np.abs(gate.sum(axis=1) - 1.0).max() <= 1e-5
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_grouping_is_bit_exact(name):
+    w = synth.WORKLOADS[name]
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    idx_np, _, _, idx, _ = _router(w, inp, dev, cfg)
+    R = moe.moe_rows_capacity(cfg)
+    E, T, k = w.n_experts, w.T, w.top_k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    src = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    xdt = dev["x"].dtype
+    x_perm = torch.zeros(R, w.d_model, dtype=xdt, device="cuda")
+    ws = moe.alloc_workspace(cfg)
+    moe.moe_permute(cfg, idx, dev["x"], counts, offsets, dest, src, x_perm, ws)
+    assert moe.moe_get_device_error(ws) == moe.MOE_OK
+    ref = O.dispatch(idx_np, E, O.capacity(T, k, E, w.capacity_factor))
+    assert (counts.cpu().numpy() == ref.counts).all()
+    assert (offsets.cpu().numpy() == ref.offsets).all()
+    assert (dest.cpu().numpy() == ref.dest_row).all()
+    P = int(ref.offsets[-1])
+    assert (src.cpu().numpy()[:P] == ref.src_token).all()
+    xp = x_perm[:P].cpu()
+    xr = dev["x"].cpu()[torch.from_numpy(ref.src_token.astype(np.int64))]
+    assert torch.equal(xp.view(torch.int16) if xdt == torch.bfloat16 else xp.view(torch.int32),
+                       xr.view(torch.int16) if xdt == torch.bfloat16 else xr.view(torch.int32))
+    if w.capacity_factor > 0:
+        assert (dest.cpu().numpy() < 0).sum() == T * k - P
+
+
+def _grouped(w, inp, dev, cfg):
+    idx_np, gate_np, _, idx, gate = _router(w, inp, dev, cfg)
+    R = moe.moe_rows_capacity(cfg)
+    rows = moe.moe_grouped_rows(cfg)
+    E, T, k = w.n_experts, w.T, w.top_k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    src = torch.empty(R, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(R, w.d_model, dtype=dev["x"].dtype, device="cuda")
+    y = torch.full((rows, w.d_model), float("nan"), dtype=dev["x"].dtype, device="cuda")
+    ws = moe.alloc_workspace(cfg)
+    moe.moe_permute(cfg, idx, dev["x"], counts, offsets, dest, src, x_perm, ws)
+    moe.moe_grouped_ffn(cfg, x_perm, offsets, dev["x"], dev["w_gate"], dev["w_up"], dev["w_down"], y, ws)
+    assert moe.moe_get_device_error(ws) == moe.MOE_OK
+    return dict(idx=idx_np, gate=gate_np, gate_t=gate, offsets=offsets.cpu().numpy(), src=src.cpu().numpy(),
+                dest=dest, dest_np=dest.cpu().numpy(), y=y, R=R, ws=ws)
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_grouped_ffn_matches_oracle(name):
+    w = synth.WORKLOADS[name]
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    g = _grouped(w, inp, dev, cfg)
+    y = to_f64(g["y"])
+    off, src, R = g["offsets"], g["src"], g["R"]
+    x64 = inp.f64["x"]
+    for e in range(w.n_experts):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        ref = O.expert_mlp(x64[src[lo:hi]], *inp.expert(e))
+        assert_close(y[lo:hi], ref, out_tolerance(w), f"{name} expert {e}")
+    for s in range(w.n_shared):
+        ref = O.expert_mlp(x64, *inp.expert(w.n_experts + s))
+        assert_close(y[R + s * w.T:R + (s + 1) * w.T], ref, out_tolerance(w), f"{name} shared")
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_combine_matches_oracle(name):
+    w = synth.WORKLOADS[name]
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    g = _grouped(w, inp, dev, cfg)
+    out = torch.empty(w.T, w.d_model, dtype=dev["x"].dtype, device="cuda")
+    moe.moe_combine(cfg, g["y"], g["dest"], g["gate_t"], out, g["ws"])
+    assert moe.moe_get_device_error(g["ws"]) == moe.MOE_OK
+    y = to_f64(g["y"])
+    R = g["R"]
+    shared = None
+    if w.n_shared:
+        shared = sum(y[R + s * w.T:R + (s + 1) * w.T] for s in range(w.n_shared))
+    ref = O.combine(g["dest_np"], g["gate"], y[:R], shared, w.d_model)
+    # only the final rounding of out (bf16: 2^-9 relative) separates the two
+    assert_close(to_f64(out), ref, 4e-3 if w.dtype == "bf16" else 1e-6, f"{name} combine")
