@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE FFN layer forward on B300: prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_layer_forward over one batch of synthetic input (router ->
+grouping -> grouped SwiGLU GEMMs -> combine). Default workload: the
+Mixtral-8x7B-shaped prefill layer (T=4096, d=4096, 8 experts, top-2, d_ff=14336).
+
+value        tokens/s with inputs resident in HBM, K steps timed with CUDA events
+             (barrier + synchronize on both sides, max over ranks); expert weights
+             (2.8 GB) exceed the 126 MB L2, so every step streams them from HBM.
+e2e          the same metric through the same C-ABI call with the activations in
+             pinned host memory: each step copies x host->device, runs the layer and
+             copies out device->host.
+roofline     the dominant kernel (the gate/up grouped GEMM), timed by events recorded
+             around it inside the timed region on the launching stream.
+cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload.
+--impl reference  times that oracle alone, step by step, on the host cores.
+N > 1 (torchrun): every rank runs its own replica of the layer (the layer has no
+exchange step), value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s on 1 B300"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mixtral_8x7b")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w, kept_pairs: int, groups_touched: int):
+    """Work of one layer forward, from the realised routing (counted, not estimated)."""
+    rows = kept_pairs + w.n_shared * w.T
+    d, F = w.d_model, w.d_ff
+    e = 2  # bytes per bf16 element
+    return {
+        "gateup_flops": 4.0 * d * F * rows,
+        "down_flops": 2.0 * d * F * rows,
+        "router_flops": 2.0 * w.T * d * w.n_experts,
+        "gateup_bytes": groups_touched * 2.0 * F * d * e + rows * d * e + rows * F * e,
+        "down_bytes": groups_touched * 1.0 * d * F * e + rows * F * e + rows * d * e,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.tmp.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.tmp.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in ("gemm_tc.cu", "tc_ptx.cuh"):
+        with open(os.path.join(ROOT, "sparse_expert_mlp_router_b300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the gate/up GEMM from a committed ncu capture, if that capture
+    was taken of the current kernel source; otherwise None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload)
+    if not e or e.get("source_sha256") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------- the CPU oracle
+
+def oracle_sample(w, n_tokens: int, one_token_batches: bool):
+    """Returns (callable that runs the oracle once, tokens it covers, description).
+
+    The expert weights are generated on the host and converted to float64 before the
+    timing starts; the timed call is the oracle's layer forward alone.
+    """
+    import numpy as np
+    import oracle as O
+    import synth
+
+    x64 = synth.as_f64(synth.host_tensor(w, "x"), w.dtype)
+    wr64 = synth.as_f64(synth.host_tensor(w, "w_router"), w.dtype)
+    bias = synth.router_bias(w.n_experts, w.bias_s)
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
+    if one_token_batches:
+        assert w.capacity_factor <= 0, "a one-token batch changes capacity; use a dropless workload"
+        need = set()
+        idx, _, _ = O.route(x64[toks], wr64, bias, w.top_k, w.score, w.renormalize)
+        need |= set(np.unique(idx).tolist())
+    else:
+        idx, _, _ = O.route(x64, wr64, bias, w.top_k, w.score, w.renormalize)
+        need = set(np.unique(idx[toks]).tolist())
+    need |= set(range(w.n_experts, w.n_experts + w.n_shared))
+    cache = {g: tuple(synth.as_f64(a, w.dtype) for a in synth.host_expert(w, g)) for g in sorted(need)}
+    experts = cache.__getitem__
+    kw = dict(top_k=w.top_k, score=w.score, renormalize=w.renormalize, capacity_factor=w.capacity_factor,
+              n_shared=w.n_shared)
+    if one_token_batches:
+        state = {"i": 0}
+
+        def run():
+            t = toks[state["i"] % len(toks)]
+            state["i"] += 1
+            O.layer_forward(x64[t:t + 1], wr64, bias, experts, **kw)
+            return 1
+        desc = f"{w.name}: one token per step (a 1-token dropless batch), tokens drawn from the {w.T}-token batch"
+    else:
+        def run():
+            O.layer_forward(x64, wr64, bias, experts, tokens=toks, **kw)
+            return len(toks)
+        desc = (f"{w.name}: routing and grouping of all {w.T} tokens, expert MLPs and combine for "
+                f"{len(toks)} sampled tokens")
+    return run, desc
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    run, desc = oracle_sample(w, max(args.steps + args.warmup, 1), one_token_batches=True)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        n += run()
+    dt = time.perf_counter() - t0
+    value = n / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
+                   "top_k": w.top_k, "d_ff": w.d_ff},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- our layer
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import synth
+    import sparse_expert_mlp_router_b300 as moe
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    cfg = moe.make_config(T=w.T, d_model=w.d_model, n_experts=w.n_experts, top_k=w.top_k, d_ff=w.d_ff,
+                          n_shared=w.n_shared, score=w.score, renormalize=w.renormalize,
+                          capacity_factor=w.capacity_factor, dtype=w.dtype)
+    dev = synth.device_inputs(w)
+    ws = moe.alloc_workspace(cfg)
+    dt = dev["x"].dtype
+    out = torch.empty(w.T, w.d_model, dtype=dt, device="cuda")
+    counts = torch.empty(w.n_experts, dtype=torch.int32, device="cuda")
+    args_fwd = (cfg, dev["x"], dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"], out, ws)
+
+    # one checked forward: status and the realised routing (kept pairs, experts touched)
+    moe.moe_layer_forward(*args_fwd, counts_out=counts)
+    status = moe.moe_get_device_error(ws)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.status_string(status)}")
+    cap = moe.moe_capacity(cfg)
+    c = counts.cpu().numpy()
+    kept = int(np.minimum(c, cap).sum())
+    touched = int((np.minimum(c, cap) > 0).sum()) + w.n_shared
+    work = algorithmic(w, kept, touched)
+
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for i in range(W):
+        moe.moe_layer_forward_timed(*args_fwd, evs[i % K])
+    barrier()
+    props = torch.cuda.get_device_properties(local)
+    try:
+        gpu_id = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except AttributeError:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        moe.moe_layer_forward_timed(*args_fwd, evs[i])
+    t_end.record()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])   # [K, 5] ms
+    status = moe.moe_get_device_error(ws)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(status)}")
+    max_ms = elapsed_ms
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        max_ms = float(t.item())
+    value = w.T * K * world / (max_ms / 1e3)
+
+    # end to end: activations in pinned host memory, copies inside the timed region
+    x_host = dev["x"].cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=dt).pin_memory()
+    x_dev = torch.empty_like(dev["x"])
+    args_e2e = (cfg, x_dev, dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"], out, ws)
+    K2 = max(args.e2e_steps, 1)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(*args_e2e)
+        out_host.copy_(out, non_blocking=True)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(*args_e2e)
+        out_host.copy_(out, non_blocking=True)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = w.T * K2 * world / (e2e_ms / 1e3)
+    if moe.moe_get_device_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device status after e2e timing")
+
+    # roofline of the dominant kernel: the gate/up grouped GEMM (stage 2 -> 3)
+    peaks, peak_src = load_peaks()
+    gemm_ms = float(stage[:, 2].mean())
+    t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_bytes:
+        achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = measured_traffic(w.name)
+    roof["kernel"] = "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)"
+    roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else f"{peak_src} copy bandwidth"
+    roof["ms_per_launch"] = gemm_ms
+
+    stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
+                         [float(v) for v in stage.mean(axis=0)]))
+    gemm_tflops = (work["gateup_flops"] + work["down_flops"]) / ((stage[:, 2] + stage[:, 3]).mean() / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        run, desc = oracle_sample(w, args.cpu_sample_tokens, one_token_batches=False)
+        t0 = time.perf_counter()
+        n = run()
+        dtc = time.perf_counter() - t0
+        cpu = {"value": n / dtc, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+               "seconds": dtc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
+                   "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff, "score": w.score,
+                   "capacity_factor": w.capacity_factor, "kept_pairs": kept, "groups_touched": touched,
+                   "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step"
+                         % (touched * 3.0 * w.d_model * w.d_ff * 2 / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+        "gpu_launches": K * moe.moe_layer_launch_count(cfg),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "stages_ms": stages_ms,
+        "grouped_gemm_tflops": gemm_tflops,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -184,7 +184,7 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
 /*
  * moe_layer_forward that also records CUDA events between its stages, for timing:
  * events[0] before the router, [1] after the router, [2] after the grouping (histogram,
- * scan, scatter, row gather), [3] after the gate/up GEMM, [4] after the down GEMM,
+ * scan, scatter, row gather, group schedule), [3] after the gate/up GEMM, [4] after the down GEMM,
  * [5] after the combine. `events` holds n_events cudaEvent_t handles (n_events <= 6;
  * the first n_events boundaries are recorded).
  */
@@ -193,6 +193,9 @@ moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, con
                                      const void* w_down, void* out, int32_t* topk_idx_out,
                                      int32_t* counts_out, void* ws, size_t ws_bytes,
                                      void* const* events, int32_t n_events, cudaStream_t stream);
+
+/* Number of kernel launches one moe_layer_forward call enqueues for this configuration (-1 if invalid). */
+int32_t moe_layer_launch_count(const moe_config_t* cfg);
 
 /*
  * Synchronise `stream`, then return the first device-side status recorded in the workspace

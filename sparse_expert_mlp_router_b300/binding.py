@@ -22,7 +22,7 @@ EXPORTS = [
     "moe_status_string", "moe_check_config", "moe_capacity", "moe_rows_capacity", "moe_grouped_rows",
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
-    "moe_clear_device_error", "moe_selftest_bounded_wait",
+    "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
 ]
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "moe_get_device_error": ([_vp, _vp], i32),
             "moe_clear_device_error": ([_vp, _vp], i32),
             "moe_selftest_bounded_wait": ([_vp, sz, u64, _vp], i32),
+            "moe_layer_launch_count": ([_cfgp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -132,6 +133,10 @@ def moe_grouped_rows(cfg: MoeConfig) -> int:
 
 def moe_workspace_size(cfg: MoeConfig) -> int:
     return lib().moe_workspace_size(ctypes.byref(cfg))
+
+
+def moe_layer_launch_count(cfg: MoeConfig) -> int:
+    return lib().moe_layer_launch_count(ctypes.byref(cfg))
 
 
 # -------------------------------------------------------------- workspace
@@ -198,6 +203,9 @@ def moe_layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, ws, top
 def moe_layer_forward_timed(cfg, x, w_router, bias, w_gate, w_up, w_down, out, ws, events,
                             topk_idx_out=None, counts_out=None, stream=None) -> None:
     """events: up to 6 torch.cuda.Event(enable_timing=True) recorded at the stage boundaries."""
+    for e in events:
+        if e.cuda_event == 0:        # torch creates the CUDA event on its first record
+            e.record()
     handles = (_vp * len(events))(*[e.cuda_event for e in events])
     _check(lib().moe_layer_forward_timed(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(w_gate),
                                          _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx_out),

@@ -68,7 +68,6 @@ __global__ void group_hist_kernel(const int32_t* __restrict__ idx, int T, int k,
 // total counts, capacity clamp, exclusive scan of the kept counts over experts.
 __global__ void group_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int cap,
                                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int32_t kept[kMaxExperts];
   __shared__ int32_t warp_tot[kMaxExperts / 32];
   const int e = threadIdx.x;
   int run = 0;
@@ -93,10 +92,7 @@ __global__ void group_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunk
   __syncthreads();
   int base = 0;
   for (int w = 0; w < warp; ++w) base += warp_tot[w];
-  if (e < E) {
-    kept[e] = kv;
-    offsets[e] = base + incl - kv;
-  }
+  if (e < E) offsets[e] = base + incl - kv;
   if (e == blockDim.x - 1) offsets[E] = base + incl;
 }
 

@@ -153,14 +153,17 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
   return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
 }
 
-cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const int32_t* offsets,
-                    const void* x, const void* wg, const void* wu, const void* wd, void* y, cudaStream_t st,
-                    cudaEvent_t mid_event) {
+// Group schedule from the offsets (one small kernel), then the two contractions.
+cudaError_t run_schedule(const Shape& s, const WsLayout& L, void* ws, const int32_t* offsets, cudaStream_t st) {
+  return launch_group_schedule(s, offsets, at<void>(ws, L.sched), at<int32_t>(ws, L.status), st);
+}
+
+cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const void* x, const void* wg,
+                    const void* wu, const void* wd, void* y, cudaStream_t st, cudaEvent_t mid_event) {
   int32_t* status = at<int32_t>(ws, L.status);
   void* sched = at<void>(ws, L.sched);
   void* h = at<void>(ws, L.h);
   cudaError_t e;
-  if ((e = launch_group_schedule(s, offsets, sched, status, st)) != cudaSuccess) return e;
   if (s.dtype == MOE_BF16) {
     if ((e = launch_gemm_gateup_tc(s, x_perm, x, wg, wu, sched, h, status, st)) != cudaSuccess) return e;
     if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
@@ -168,6 +171,13 @@ cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_p
   }
   if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
   return launch_ffn_fma(s, x_perm, x, wg, wu, wd, sched, h, y, st);
+}
+
+// Kernel launches one moe_layer_forward enqueues.
+int layer_launches(const Shape& s) {
+  const int router = 1, grouping = 4, schedule = 1, mlp = 2, combine = 1;
+  (void)s;
+  return router + grouping + schedule + mlp + combine;
 }
 
 moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
@@ -198,18 +208,18 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   void* x_perm = at<void>(ws, L.x_perm);
   void* y = at<void>(ws, L.y);
 
-  cudaError_t e = cudaSuccess;
-  if (ev[0] && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((e = run_router(s, x, w_router, bias, idx, gate, nullptr, status, st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if (ev[1] && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((e = run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, st)) != cudaSuccess)
+  auto mark = [&](int i) { return ev[i] == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(1)) return MOE_ERR_CUDA;
+  if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (ev[2] && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((e = run_ffn(s, L, ws, x_perm, offsets, x, w_gate, w_up, w_down, y, st, ev[3])) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (ev[4] && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((e = launch_combine(s, y, dest_row, gate, out, status, st)) != cudaSuccess) return MOE_ERR_CUDA;
-  if (ev[5] && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (run_schedule(s, L, ws, offsets, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(2)) return MOE_ERR_CUDA;
+  if (run_ffn(s, L, ws, x_perm, x, w_gate, w_up, w_down, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(4)) return MOE_ERR_CUDA;
+  if (launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(5)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -310,8 +320,10 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const 
     return MOE_ERR_INVALID_ARG;
   const Shape s = make_shape(*cfg);
   if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
-  return cuda_status(run_ffn(s, make_layout(s), ws, x_perm, offsets, x ? x : x_perm, w_gate, w_up, w_down, y_perm,
-                             stream, nullptr));
+  const WsLayout L = make_layout(s);
+  cudaError_t e = run_schedule(s, L, ws, offsets, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_ffn(s, L, ws, x_perm, x ? x : x_perm, w_gate, w_up, w_down, y_perm, stream, nullptr));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* dest_row,
@@ -341,6 +353,11 @@ moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, con
                                      size_t ws_bytes, void* const* events, int32_t n_events, cudaStream_t stream) {
   return layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, topk_idx_out, counts_out, ws, ws_bytes,
                        events, n_events, stream);
+}
+
+int32_t moe_layer_launch_count(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  return layer_launches(make_shape(*cfg));
 }
 
 moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns, cudaStream_t stream) {

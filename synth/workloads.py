@@ -70,6 +70,9 @@ WORKLOADS = {
         Workload("mini_deepseek", T=257, d_model=512, n_experts=48, top_k=6, d_ff=256, n_shared=1,
                  score="sigmoid", capacity_factor=1.25, bias_s=1.2),
         Workload("mini_decode", T=5, d_model=256, n_experts=64, top_k=8, d_ff=128),
+        # Mixtral-shaped tiles on two experts (0.7 GB of weights): small enough for a
+        # many-pass profiler capture, still far larger than L2
+        Workload("prof_mixtral_e2", T=2048, d_model=4096, n_experts=2, top_k=2, d_ff=14336),
     ]
 }
 
