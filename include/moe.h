@@ -141,6 +141,27 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
                          void* x_perm, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * moe_permute for callers that cannot allocate device memory: code that enqueues work while
+ * a stream is being captured into a CUDA graph, a plug-in whose host framework owns all
+ * device memory and passes in only the call's tensors, a real-time loop that must not touch
+ * the allocator. The source pages have no counterpart; this is an interface of this library.
+ *   Same arguments and results as moe_permute, without ws / ws_bytes, plus
+ *   status  device int32 or NULL: a device-side problem (an id outside [0, E)) is recorded
+ *           here with an atomic compare-and-swap from 0, so zero it before the call.
+ * The per-chunk expert histogram lives in a fixed 256 KiB array in libmoe.so's own device
+ * memory, held by every GPU that loads the library until the process exits. It fits
+ * ceil(T/128) * E <= 65536 (T <= 32768 at E = 256); larger configurations return
+ * MOE_ERR_WORKSPACE before anything is enqueued. Nothing is allocated or freed. The first
+ * call on a device looks up the array's device address: make it before any stream capture.
+ * All calls share the array and leave their contents in it; calls that overlap on the GPU
+ * (unordered streams) race and give wrong results.
+ */
+moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_idx, const void* x,
+                                 int32_t* counts, int32_t* offsets, int32_t* dest_row,
+                                 int32_t* src_token, void* x_perm, int32_t* status,
+                                 cudaStream_t stream);
+
+/*
  * Grouped expert MLPs [KG definition: "grouped GEMMs on each expert's batch"; TB "Experts as
  * Specialized Subnetworks"]: for every routed expert e and kept row r in
  * [offsets[e], offsets[e+1]) and, for the shared expert, every token t:

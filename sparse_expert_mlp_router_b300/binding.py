@@ -23,6 +23,7 @@ EXPORTS = [
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
     "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
+    "moe_permute_noalloc",
 ]
 
 
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
             "moe_clear_device_error": ([_vp, _vp], i32),
             "moe_selftest_bounded_wait": ([_vp, sz, u64, _vp], i32),
             "moe_layer_launch_count": ([_cfgp], i32),
+            "moe_permute_noalloc": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -180,6 +182,14 @@ def moe_permute(cfg, topk_idx, x, counts, offsets, dest_row, src_token, x_perm, 
     _check(lib().moe_permute(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
                              _ptr(dest_row), _ptr(src_token), _ptr(x_perm), _ptr(ws), ws.numel(),
                              _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, topk_idx, x, counts, offsets, dest_row, src_token, x_perm, status=None,
+                        stream=None) -> None:
+    """moe_permute without a workspace, for callers that cannot allocate device memory (see moe.h)."""
+    _check(lib().moe_permute_noalloc(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
+                                     _ptr(dest_row), _ptr(src_token), _ptr(x_perm), _ptr(status),
+                                     _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_grouped_ffn(cfg, x_perm, offsets, x, w_gate, w_up, w_down, y_perm, ws, stream=None) -> None:
