@@ -30,11 +30,9 @@
 // Every wait is bounded: a stall records MOE_ERR_TIMEOUT, all roles leave
 // their loops, in-flight copies and MMAs are drained with bounded waits, and
 // the TMEM is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "internal.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 namespace {
@@ -328,32 +326,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 // ------------------------------------------------------------------ host ---
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2D bf16 map over a row-major [rows, inner] tensor, box {64, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int MODE, int BN>
 cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& b2,
                            const GemmArgs& args, int64_t max_tiles, cudaStream_t st) {
@@ -379,10 +351,10 @@ cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void
                                   const void* w_up, const void* sched, void* h, int32_t* status, cudaStream_t st) {
   CUtensorMap a, a2, b, b2;
   const uint64_t R = (uint64_t)(s.R > 0 ? s.R : 1);
-  if (!make_map(&a, x_perm, s.d, R, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&a2, s.S > 0 ? x : x_perm, s.d, s.S > 0 ? (uint64_t)s.T : R, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&b, w_gate, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&b2, w_up, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&a, x_perm, s.d, R, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&a2, s.S > 0 ? x : x_perm, s.d, s.S > 0 ? (uint64_t)s.T : R, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&b, w_gate, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&b2, w_up, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
   GemmArgs args{};
   args.K = s.d;
   args.n_tiles = s.F / 128;
@@ -401,8 +373,8 @@ cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_dow
   CUtensorMap a, b;
   const uint64_t rows = (uint64_t)s.R + (uint64_t)s.S * s.T;
   const int bn = (s.d % 256 == 0) ? 256 : 128;
-  if (!make_map(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&b, w_down, s.F, (uint64_t)s.G * s.d, (uint32_t)bn)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&b, w_down, s.F, (uint64_t)s.G * s.d, (uint32_t)bn)) return cudaErrorInvalidValue;
   GemmArgs args{};
   args.K = s.F;
   args.n_tiles = s.d / bn;

@@ -80,6 +80,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // Each returns cudaGetLastError() after enqueueing.
 cudaError_t launch_router_fma(const Shape& s, const void* x, const void* w, const float* bias,
                               int32_t* idx, float* gate, float* scores, cudaStream_t st);
+bool router_tc_supported(const Shape& s);
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const float* bias,
                              int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st);
 

@@ -137,7 +137,7 @@ inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_O
 // The stage bodies, shared by the stage entry points and the whole-layer call.
 cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
                        float* gate, float* scores, int32_t* status, cudaStream_t st) {
-  (void)status;
+  if (router_tc_supported(s)) return launch_router_tc(s, x, w_router, bias, idx, gate, scores, status, st);
   return launch_router_fma(s, x, w_router, bias, idx, gate, scores, st);
 }
 

@@ -31,7 +31,22 @@ def _router(w, inp, dev, cfg):
 
 @pytest.mark.parametrize("name", MINI)
 def test_router_matches_oracle(name):
-    w = synth.WORKLOADS[name]
+    _check_router(synth.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("edit", [
+    dict(T=1, n_experts=1, top_k=1),                        # one token, one expert
+    dict(T=130, n_experts=6, top_k=3),                      # E below one 16-column MMA slice
+    dict(T=257, n_experts=200, top_k=8, bias_s=1.2),        # E not a multiple of 16 or 32, skewed
+    dict(T=64, n_experts=256, top_k=8, score="sigmoid"),    # the widest accumulator
+    dict(T=129, n_experts=17, top_k=5, renormalize=False),  # raw softmax gates
+    dict(T=40, n_experts=33, top_k=2, score="sigmoid", renormalize=False, bias_s=0.5),
+])
+def test_router_shapes(edit):
+    _check_router(synth.WORKLOADS["mini_qwen3"].with_(**edit))
+
+
+def _check_router(w):
     inp = Inputs(w)
     dev = inp.device()
     cfg = cfg_of(w)
@@ -136,3 +151,18 @@ def test_combine_matches_oracle(name):
     ref = O.combine(g["dest_np"], g["gate"], y[:R], shared, w.d_model)
     # only the final rounding of out (bf16: 2^-9 relative) separates the two
     assert_close(to_f64(out), ref, 4e-3 if w.dtype == "bf16" else 1e-6, f"{name} combine")
+
+
+def test_router_nan_token_gets_distinct_ids():
+    # a token whose logits are all NaN still gets k distinct ids in [0, E); the others are unaffected
+    w = synth.WORKLOADS["mini_qwen3"].with_(T=150, n_experts=40, top_k=8)
+    inp = Inputs(w)
+    dev = inp.device()
+    dev["x"][3] = float("nan")
+    idx, gate, _, _, _ = _router(w, inp, dev, cfg_of(w))
+    row = idx[3]
+    assert len(set(row.tolist())) == w.top_k and ((row >= 0) & (row < w.n_experts)).all()
+    keep = np.ones(w.T, dtype=bool)
+    keep[3] = False
+    ref_scores = O.scores_from_logits(O.router_logits(inp.f64["x"], inp.f64["w_router"], inp.bias), w.score)
+    check_routing(idx[keep], ref_scores[keep], w.top_k)
