@@ -10,6 +10,9 @@ Mixtral-8x7B-shaped prefill layer (T=4096, d=4096, 8 experts, top-2, d_ff=14336)
 value        tokens/s with inputs resident in HBM, K steps timed with CUDA events
              (barrier + synchronize on both sides, max over ranks); expert weights
              (2.8 GB) exceed the 126 MB L2, so every step streams them from HBM.
+             The K moe_layer_forward calls are captured into one CUDA graph and
+             replayed (--eager: K separate calls); each captured call enqueues the
+             same kernels as an eager one.
 e2e          the same metric through the same C-ABI call with the activations in
              pinned host memory: each step copies x host->device, runs the layer and
              copies out device->host.
@@ -53,6 +56,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--eager", action="store_true",
+                    help="time K separate launches of the layer instead of one CUDA-graph replay of K layers")
     return ap.parse_args()
 
 
@@ -289,9 +294,20 @@ def run_ours(args, w):
 
     K, W = args.steps, args.warmup
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:            # create every event before any capture
+        for e in row:
+            e.record()
     for i in range(W):
         moe.moe_layer_forward_timed(*args_fwd, evs[i % K])
     barrier()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(K):
+                moe.moe_layer_forward_timed(*args_fwd, evs[i])
+        graph.replay()         # one untimed replay
+        barrier()
     props = torch.cuda.get_device_properties(local)
     try:
         gpu_id = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
@@ -303,8 +319,11 @@ def run_ours(args, w):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for i in range(K):
-        moe.moe_layer_forward_timed(*args_fwd, evs[i])
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(K):
+            moe.moe_layer_forward_timed(*args_fwd, evs[i])
     t_end.record()
     barrier()
     clocks = sampler.stop()
@@ -388,7 +407,8 @@ def run_ours(args, w):
                    "capacity_factor": w.capacity_factor, "kept_pairs": kept, "groups_touched": touched,
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step"
                          % (touched * 3.0 * w.d_model * w.d_ff * 2 / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": "eager" if args.eager else "cuda_graph"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
         "gpu_launches": K * moe.moe_layer_launch_count(cfg),

@@ -15,22 +15,16 @@
 // with float32 FMAs; tensor cores have no float32 mode precise enough for
 // float32 layers. It serves layers stored in float32.
 #include "internal.cuh"
+#include "sched.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;
-
-// One warp. Groups are processed 32 at a time with a warp prefix sum.
+// One warp: checks offsets supplied by the caller (offsets[0] == 0, non-decreasing,
+// offsets[E] <= R), then builds the schedule.
 __global__ void group_schedule_kernel(const int32_t* __restrict__ offsets, int E, int S, int T, int64_t R,
                                       int32_t* __restrict__ sched, int32_t* status) {
-  const int G = E + S;
-  int32_t* tile_start = sched;
-  int32_t* a_row = sched + (G + 1);
-  int32_t* out_row = a_row + G;
-  int32_t* rows = out_row + G;
   const int lane = threadIdx.x;
-  // validate: offsets[0] == 0, non-decreasing, offsets[E] <= R
   bool bad = false;
   for (int g = lane; g < E; g += 32) {
     const int lo = offsets[g], hi = offsets[g + 1];
@@ -38,35 +32,7 @@ __global__ void group_schedule_kernel(const int32_t* __restrict__ offsets, int E
   }
   bad = __any_sync(0xffffffffu, bad);
   if (bad && lane == 0) set_status(status, MOE_ERR_DEVICE_INDEX);
-  int carry = 0;
-  for (int base = 0; base < G; base += 32) {
-    const int g = base + lane;
-    int ar = 0, orow = 0, nr = 0;
-    if (g < E) {
-      ar = bad ? 0 : offsets[g];
-      orow = ar;
-      nr = bad ? 0 : offsets[g + 1] - offsets[g];
-    } else if (g < G) {
-      ar = 0;
-      orow = (int)(R + (int64_t)(g - E) * T);
-      nr = T;
-    }
-    const int tiles = (nr + kBM - 1) / kBM;
-    int incl = tiles;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (g < G) {
-      tile_start[g] = carry + incl - tiles;
-      a_row[g] = ar;
-      out_row[g] = orow;
-      rows[g] = nr;
-    }
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) tile_start[G] = carry;
+  build_schedule_warp(offsets, bad, E, S, T, R, sched);
 }
 
 __device__ __forceinline__ float silu_precise(float z) { return z / (1.0f + expf(-z)); }

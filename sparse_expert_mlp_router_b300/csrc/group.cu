@@ -16,6 +16,7 @@
 // pair's rank inside the chunk is a popcount of the mask bits below its token;
 // a per-expert prefix over chunks then gives the global rank.
 #include "internal.cuh"
+#include "sched.cuh"
 
 namespace moe {
 namespace {
@@ -64,23 +65,40 @@ __global__ void group_hist_kernel(const int32_t* __restrict__ idx, int T, int k,
   }
 }
 
-// One CTA: per expert, exclusive prefix over chunks (in place: counts -> rank base),
-// total counts, capacity clamp, exclusive scan of the kept counts over experts.
-__global__ void group_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int cap,
-                                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int32_t warp_tot[kMaxExperts / 32];
+// One CTA of 256 threads (one per expert): per expert, exclusive prefix over chunks
+// (in place: counts -> rank base), total counts, capacity clamp, exclusive scan of
+// the kept counts over experts; optionally the group schedule of the grouped GEMMs.
+// Chunk counts are staged through shared memory 32 chunks at a time, so the loads
+// of a tile are all in flight together.
+constexpr int kScanThreads = 256;
+constexpr int kScanTile = 32;
+
+__global__ void __launch_bounds__(kScanThreads)
+group_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int cap, int32_t* __restrict__ counts,
+                  int32_t* __restrict__ offsets, int32_t* __restrict__ sched, int S, int T, int64_t R) {
+  __shared__ int32_t tile[kScanTile * kMaxExperts];
+  __shared__ int32_t warp_tot[kScanThreads / 32];
+  __shared__ int32_t s_off[kMaxExperts + 1];
   const int e = threadIdx.x;
   int run = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = chunk_counts[(size_t)c * E + e];
-      chunk_counts[(size_t)c * E + e] = run;
-      run += v;
-    }
-    counts[e] = run;
+  for (int c0 = 0; c0 < nchunks; c0 += kScanTile) {
+    const int nc = min(kScanTile, nchunks - c0);
+    int32_t* g = chunk_counts + (size_t)c0 * E;
+    for (int i = threadIdx.x; i < nc * E; i += kScanThreads) tile[i] = g[i];
+    __syncthreads();
+    if (e < E)
+      for (int c = 0; c < nc; ++c) {
+        const int v = tile[c * E + e];
+        tile[c * E + e] = run;
+        run += v;
+      }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nc * E; i += kScanThreads) g[i] = tile[i];
+    __syncthreads();
   }
+  if (e < E) counts[e] = run;
   const int kv = (e < E) ? min(run, cap) : 0;
-  // block-wide exclusive scan of kv over the (up to 256) experts
+  // block-wide exclusive scan of kv over the experts
   const int lane = e & 31, warp = e >> 5;
   int incl = kv;
 #pragma unroll
@@ -92,8 +110,18 @@ __global__ void group_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunk
   __syncthreads();
   int base = 0;
   for (int w = 0; w < warp; ++w) base += warp_tot[w];
-  if (e < E) offsets[e] = base + incl - kv;
-  if (e == blockDim.x - 1) offsets[E] = base + incl;
+  if (e < E) {
+    offsets[e] = base + incl - kv;
+    s_off[e] = base + incl - kv;
+  }
+  if (e == kScanThreads - 1) {
+    offsets[E] = base + incl;
+    s_off[E] = base + incl;
+  }
+  if (sched != nullptr) {
+    __syncthreads();
+    if (warp == 0) build_schedule_warp(s_off, false, E, S, T, R, sched);
+  }
 }
 
 __global__ void group_scatter_kernel(const int32_t* __restrict__ idx, int T, int k, int E,
@@ -150,9 +178,9 @@ cudaError_t launch_group_hist(const Shape& s, const int32_t* idx, int32_t* chunk
 }
 
 cudaError_t launch_group_scan(const Shape& s, int32_t* chunk_counts, int32_t* counts, int32_t* offsets,
-                              cudaStream_t st) {
-  const int threads = ((s.E + 31) / 32) * 32;
-  group_scan_kernel<<<1, threads, 0, st>>>(chunk_counts, s.nchunks, s.E, s.cap, counts, offsets);
+                              void* sched, cudaStream_t st) {
+  group_scan_kernel<<<1, kScanThreads, 0, st>>>(chunk_counts, s.nchunks, s.E, s.cap, counts, offsets,
+                                                static_cast<int32_t*>(sched), s.S, s.T, s.R);
   return cudaGetLastError();
 }
 

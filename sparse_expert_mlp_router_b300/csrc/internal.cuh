@@ -86,8 +86,9 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const
 
 cudaError_t launch_group_hist(const Shape& s, const int32_t* idx, int32_t* chunk_counts,
                               int32_t* status, cudaStream_t st);
+// sched: NULL, or the workspace group schedule to build from the new offsets
 cudaError_t launch_group_scan(const Shape& s, int32_t* chunk_counts, int32_t* counts,
-                              int32_t* offsets, cudaStream_t st);
+                              int32_t* offsets, void* sched, cudaStream_t st);
 cudaError_t launch_group_scatter(const Shape& s, const int32_t* idx, const int32_t* chunk_base,
                                  const int32_t* offsets, int32_t* dest_row, int32_t* src_token,
                                  cudaStream_t st);

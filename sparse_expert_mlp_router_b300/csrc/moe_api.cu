@@ -134,6 +134,16 @@ moe_status_t check_ws(const Shape& s, const void* ws, size_t ws_bytes) {
 
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// A timing event: recorded as an external event node when the stream is being captured
+// into a CUDA graph, so that replays record it (a plain record would only order nodes).
+inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 // The stage bodies, shared by the stage entry points and the whole-layer call.
 cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
                        float* gate, float* scores, int32_t* status, cudaStream_t st) {
@@ -141,14 +151,18 @@ cudaError_t run_router(const Shape& s, const void* x, const void* w_router, cons
   return launch_router_fma(s, x, w_router, bias, idx, gate, scores, st);
 }
 
+// with_schedule: the scan also builds the group schedule of the grouped GEMMs (the
+// whole-layer call); the permute stage call leaves it to moe_grouped_ffn.
 cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx, const void* x,
                         int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_token, void* x_perm,
-                        cudaStream_t st) {
+                        bool with_schedule, cudaStream_t st) {
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
   cudaError_t e;
   if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
-  if ((e = launch_group_scan(s, cc, counts, offsets, st)) != cudaSuccess) return e;
+  if ((e = launch_group_scan(s, cc, counts, offsets, with_schedule ? at<void>(ws, L.sched) : nullptr, st)) !=
+      cudaSuccess)
+    return e;
   if ((e = launch_group_scatter(s, idx, cc, offsets, dest_row, src_token, st)) != cudaSuccess) return e;
   return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
 }
@@ -166,18 +180,19 @@ cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_p
   cudaError_t e;
   if (s.dtype == MOE_BF16) {
     if ((e = launch_gemm_gateup_tc(s, x_perm, x, wg, wu, sched, h, status, st)) != cudaSuccess) return e;
-    if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+    if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
     return launch_gemm_down_tc(s, h, wd, sched, y, status, st);
   }
-  if (mid_event && (e = cudaEventRecord(mid_event, st)) != cudaSuccess) return e;
+  if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
   return launch_ffn_fma(s, x_perm, x, wg, wu, wd, sched, h, y, st);
 }
 
 // Kernel launches one moe_layer_forward enqueues.
 int layer_launches(const Shape& s) {
-  const int router = 1, grouping = 4, schedule = 1, mlp = 2, combine = 1;
+  // hist, scan (+ group schedule), scatter, gather
+  const int router = 1, grouping = 4, mlp = 2, combine = 1;
   (void)s;
-  return router + grouping + schedule + mlp + combine;
+  return router + grouping + mlp + combine;
 }
 
 moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
@@ -208,13 +223,12 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   void* x_perm = at<void>(ws, L.x_perm);
   void* y = at<void>(ws, L.y);
 
-  auto mark = [&](int i) { return ev[i] == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
+  auto mark = [&](int i) { return ev[i] == nullptr || record_event(ev[i], st) == cudaSuccess; };
   if (!mark(0)) return MOE_ERR_CUDA;
   if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(1)) return MOE_ERR_CUDA;
-  if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, st) != cudaSuccess)
+  if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (run_schedule(s, L, ws, offsets, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(2)) return MOE_ERR_CUDA;
   if (run_ffn(s, L, ws, x_perm, x, w_gate, w_up, w_down, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(4)) return MOE_ERR_CUDA;
@@ -305,7 +319,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
   const Shape s = make_shape(*cfg);
   if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
   return cuda_status(run_permute(s, make_layout(s), ws, topk_idx, x, counts, offsets, dest_row, src_token, x_perm,
-                                 stream));
+                                 false, stream));
 }
 
 moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets, const void* x,

@@ -76,7 +76,7 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32
   int32_t* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_group_hist(s, topk_idx, scratch, status, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_group_scan(s, scratch, counts, offsets, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_group_scan(s, scratch, counts, offsets, nullptr, stream) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_group_scatter(s, topk_idx, scratch, offsets, dest_row, src_token, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_gather_rows(s, x, src_token, offsets, x_perm, stream) != cudaSuccess) return MOE_ERR_CUDA;
