@@ -165,7 +165,16 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
     const int t = src_token[r];
     const uint4* src = x + (size_t)t * vec_per_row;
     uint4* dst = x_perm + (size_t)r * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    // four 16-byte loads in flight per lane before their stores
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), e = __ldg(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = e;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
