@@ -215,6 +215,32 @@ moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, con
                                      int32_t* counts_out, void* ws, size_t ws_bytes,
                                      void* const* events, int32_t n_events, cudaStream_t stream);
 
+/*
+ * Routing telemetry of one batch [ST "Load imbalance": per-expert load, drops under a capacity
+ * limit, and for dropless serving the share of expert compute that is useful while every
+ * expert waits for the busiest one; ST "Memory vs compute, quantified": experts touched].
+ * Computed on the device from the per-expert counts of moe_permute / moe_layer_forward, so it
+ * needs no host synchronisation.
+ *   counts  device [E] int32 in: pairs routed to each expert before capacity
+ *   stats   device moe_routing_stats_t out
+ * kept[e] = min(counts[e], cap); mean_load = sum(kept) / E (float32); efficiency = mean_load /
+ * max_load (1 when no pair is kept). Negative counts are treated as 0 and flagged nowhere.
+ */
+typedef struct moe_routing_stats {
+  int32_t tokens;           /* T */
+  int32_t pairs;            /* sum of counts: routed (token, expert) pairs, T*k for valid routing */
+  int32_t kept;             /* sum of kept[e] */
+  int32_t dropped;          /* pairs - kept */
+  int32_t experts_touched;  /* experts with kept[e] > 0 */
+  int32_t max_load;         /* max over e of kept[e] */
+  int32_t capacity;         /* per-expert cap (T when dropless) */
+  float mean_load;          /* kept / E */
+  float efficiency;         /* mean_load / max_load */
+} moe_routing_stats_t;
+
+moe_status_t moe_routing_stats(const moe_config_t* cfg, const int32_t* counts, moe_routing_stats_t* stats,
+                               cudaStream_t stream);
+
 /* Number of kernel launches one moe_layer_forward call enqueues for this configuration (-1 if invalid). */
 int32_t moe_layer_launch_count(const moe_config_t* cfg);
 

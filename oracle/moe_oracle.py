@@ -64,6 +64,7 @@ __all__ = [
     "router_logits", "scores_from_logits", "select_topk", "gates_from_scores", "route",
     "capacity", "dispatch", "silu", "expert_mlp", "combine", "layer_forward", "LayerResult",
     "flops_per_pair", "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
+    "routing_stats",
 ]
 
 
@@ -307,3 +308,24 @@ def experts_touched_expected(E: int, k: int, batch: int) -> float:
 def experts_touched(idx: np.ndarray, E: int) -> int:
     """Number of distinct experts a routing reads."""
     return int(np.unique(np.asarray(idx).ravel()).size) if np.asarray(idx).size else 0
+
+
+def routing_stats(counts, T: int, cap: Optional[int]) -> dict:
+    """Load report of one batch from the per-expert counts (pairs routed before capacity).
+
+    [ST "Load imbalance": per-expert load, drops under a capacity limit, and, for dropless
+    serving, the share of expert compute that is useful while all wait for the busiest
+    expert -- read here as mean load / max load; ST "Memory vs compute, quantified":
+    the experts a batch touches.] kept[e] = min(counts[e], cap); exact fractions for the
+    mean load and the efficiency (1 when nothing is kept).
+    """
+    c = np.maximum(np.asarray(counts, dtype=np.int64), 0)
+    cap_v = T if cap is None else int(cap)
+    kept = np.minimum(c, cap_v)
+    E = c.size
+    K = int(kept.sum())
+    M = int(kept.max()) if E else 0
+    mean = Fraction(K, E)
+    return {"tokens": int(T), "pairs": int(c.sum()), "kept": K, "dropped": int(c.sum()) - K,
+            "experts_touched": int((kept > 0).sum()), "max_load": M, "capacity": cap_v,
+            "mean_load": mean, "efficiency": (mean / M) if M > 0 else Fraction(1)}

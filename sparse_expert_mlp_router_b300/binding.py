@@ -23,7 +23,7 @@ EXPORTS = [
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
     "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
-    "moe_permute_noalloc",
+    "moe_permute_noalloc", "moe_routing_stats",
 ]
 
 
@@ -31,6 +31,15 @@ class MoeError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         super().__init__(f"{where}: {status_string(code)}")
+
+
+class MoeRoutingStats(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int32), ("pairs", ctypes.c_int32), ("kept", ctypes.c_int32),
+        ("dropped", ctypes.c_int32), ("experts_touched", ctypes.c_int32), ("max_load", ctypes.c_int32),
+        ("capacity", ctypes.c_int32), ("mean_load", ctypes.c_float), ("efficiency", ctypes.c_float),
+    ]
+    FIELDS = [n for n, _ in _fields_]
 
 
 class MoeConfig(ctypes.Structure):
@@ -86,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "moe_selftest_bounded_wait": ([_vp, sz, u64, _vp], i32),
             "moe_layer_launch_count": ([_cfgp], i32),
             "moe_permute_noalloc": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
+            "moe_routing_stats": ([_cfgp, _vp, _vp, _vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -221,3 +231,22 @@ def moe_layer_forward_timed(cfg, x, w_router, bias, w_gate, w_up, w_down, out, w
                                          _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx_out),
                                          _ptr(counts_out), _ptr(ws), ws.numel(), handles, len(events),
                                          _stream(stream)), "moe_layer_forward_timed")
+
+
+def moe_routing_stats(cfg, counts, stats=None, stream=None):
+    """Routing telemetry from per-expert counts (see include/moe.h). `stats`: a device buffer of
+    at least sizeof(moe_routing_stats_t) bytes (a uint8 tensor), or None to allocate one.
+    Returns the buffer; read it with routing_stats_to_dict()."""
+    import torch
+    if stats is None:
+        stats = torch.zeros(ctypes.sizeof(MoeRoutingStats), dtype=torch.uint8, device=counts.device)
+    _check(lib().moe_routing_stats(ctypes.byref(cfg), _ptr(counts), _ptr(stats), _stream(stream)),
+           "moe_routing_stats")
+    return stats
+
+
+def routing_stats_to_dict(stats) -> dict:
+    """Host copy of a moe_routing_stats_t device buffer as a dict (synchronises)."""
+    raw = bytes(stats.cpu().numpy().tobytes())[:ctypes.sizeof(MoeRoutingStats)]
+    st = MoeRoutingStats.from_buffer_copy(raw)
+    return {n: getattr(st, n) for n in MoeRoutingStats.FIELDS}

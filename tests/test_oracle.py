@@ -353,3 +353,32 @@ def test_memory_and_flops_table_from_page():
 def test_flops_per_pair_counts_three_matrices():
     # one token through one SwiGLU expert: 3 matrices of d x F, 2 flops per multiply-add
     assert O.flops_per_pair(4096, 14336) == 2 * 3 * 4096 * 14336
+
+
+# ------------------------------------------------------------- telemetry ---
+
+def test_routing_stats_hand_case():
+    # counts (5, 0, 3, 2) with capacity 3: kept (3, 0, 3, 2) -> 8 kept, 2 dropped, 3 experts
+    # touched, busiest 3, mean 2, useful share 2/3
+    st = O.routing_stats([5, 0, 3, 2], T=5, cap=3)
+    assert (st["pairs"], st["kept"], st["dropped"], st["experts_touched"], st["max_load"]) == (10, 8, 2, 3, 3)
+    assert st["mean_load"] == 2 and st["efficiency"] == pytest.approx(2 / 3, abs=0)
+
+
+def test_routing_stats_balanced_and_empty():
+    assert O.routing_stats([4, 4, 4, 4], T=8, cap=None)["efficiency"] == 1
+    empty = O.routing_stats([0, 0, 0], T=1, cap=2)
+    assert empty["kept"] == 0 and empty["efficiency"] == 1 and empty["experts_touched"] == 0
+
+
+def test_routing_stats_agree_with_dispatch():
+    rng = _rng(7)
+    T, E, k = 200, 16, 4
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    cap = O.capacity(T, k, E, 1.0)
+    d = O.dispatch(idx, E, cap)
+    st = O.routing_stats(d.counts, T=T, cap=cap)
+    assert st["pairs"] == T * k and st["kept"] == int(d.offsets[-1]) == int(d.kept.sum())
+    assert st["dropped"] == int((d.dest_row < 0).sum())
+    assert st["experts_touched"] == O.experts_touched(idx[d.dest_row >= 0], E)
+    assert st["max_load"] <= cap

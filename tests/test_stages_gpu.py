@@ -166,3 +166,21 @@ def test_router_nan_token_gets_distinct_ids():
     keep[3] = False
     ref_scores = O.scores_from_logits(O.router_logits(inp.f64["x"], inp.f64["w_router"], inp.bias), w.score)
     check_routing(idx[keep], ref_scores[keep], w.top_k)
+
+
+@pytest.mark.parametrize("name", MINI)
+def test_routing_stats_match_oracle(name):
+    w = synth.WORKLOADS[name]
+    dev = Inputs(w).device()
+    cfg = cfg_of(w)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty(w.T, w.d_model, dtype=dev["x"].dtype, device="cuda")
+    counts = torch.empty(w.n_experts, dtype=torch.int32, device="cuda")
+    moe.moe_layer_forward(cfg, dev["x"], dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                          out, ws, counts_out=counts)
+    got = moe.routing_stats_to_dict(moe.moe_routing_stats(cfg, counts))
+    ref = O.routing_stats(counts.cpu().numpy(), T=w.T, cap=moe.moe_capacity(cfg))
+    for key in ("tokens", "pairs", "kept", "dropped", "experts_touched", "max_load", "capacity"):
+        assert got[key] == ref[key], key
+    for key in ("mean_load", "efficiency"):
+        assert abs(got[key] - float(ref[key])) <= 2.0 ** -23 * float(ref[key]), key
