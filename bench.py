@@ -56,6 +56,11 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                    help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales")
+    ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
+                    help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
+                         "write_traffic) and exit")
     ap.add_argument("--eager", action="store_true",
                     help="time K separate launches of the layer instead of one CUDA-graph replay of K layers")
     return ap.parse_args()
@@ -79,17 +84,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def algorithmic(w, kept_pairs: int, groups_touched: int):
-    """Work of one layer forward, from the realised routing (counted, not estimated)."""
+def algorithmic(w, kept_pairs: int, groups_touched: int, weight_bytes: float = 2.0):
+    """Work of one layer forward, from the realised routing (counted, not estimated).
+    weight_bytes: bytes per stored expert weight (2 for bf16, 1 for FP8 codes, whose per-row
+    float32 scales are counted too)."""
     rows = kept_pairs + w.n_shared * w.T
     d, F = w.d_model, w.d_ff
-    e = 2  # bytes per bf16 element
+    e = 2  # bytes per bf16 activation
+    scales = 4.0 if weight_bytes < 2 else 0.0
     return {
         "gateup_flops": 4.0 * d * F * rows,
         "down_flops": 2.0 * d * F * rows,
         "router_flops": 2.0 * w.T * d * w.n_experts,
-        "gateup_bytes": groups_touched * 2.0 * F * d * e + rows * d * e + rows * F * e,
-        "down_bytes": groups_touched * 1.0 * d * F * e + rows * F * e + rows * d * e,
+        "gateup_bytes": groups_touched * 2.0 * F * (d * weight_bytes + scales) + rows * d * e + rows * F * e,
+        "down_bytes": groups_touched * 1.0 * d * (F * weight_bytes + scales) + rows * F * e + rows * d * e,
     }
 
 
@@ -145,15 +153,19 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def kernel_source_hash() -> str:
+GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh"),
+                "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh")}
+
+
+def kernel_source_hash(weights: str = "bf16") -> str:
     h = hashlib.sha256()
-    for fn in ("gemm_tc.cu", "tc_ptx.cuh"):
+    for fn in GEMM_SOURCES[weights]:
         with open(os.path.join(ROOT, "sparse_expert_mlp_router_b300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic(workload: str):
+def measured_traffic(workload: str, weights: str = "bf16"):
     """DRAM bytes per launch of the gate/up GEMM from a committed ncu capture, if that capture
     was taken of the current kernel source; otherwise None."""
     try:
@@ -161,10 +173,46 @@ def measured_traffic(workload: str):
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    e = t.get(workload)
-    if not e or e.get("source_sha256") != kernel_source_hash():
+    e = t.get(workload if weights == "bf16" else workload + "+" + weights)
+    if not e or e.get("source_sha256") != kernel_source_hash(weights):
         return None
     return e.get("bytes_per_launch")
+
+
+def write_traffic(csv_dir: str, weights: str) -> None:
+    """profiles/traffic.json from one-pass ncu captures, one CSV per workload, made with
+
+        ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \\
+            --clock-control none -k regex:grouped_gemm -s 2 -c 2 --csv --log-file traffic_<workload>.csv \\
+            python bench.py --workload <workload> --steps 3 --warmup 1 --e2e-steps 1 --no-cpu-baseline \\
+            --eager [--weights fp8]
+
+    (the second layer forward's gate/up and down GEMMs). Each entry records the hash of the GEMM
+    source it was measured on; the roofline reports the traffic only while that source is unchanged.
+    """
+    import csv
+    import glob
+    out = json.load(open(TRAFFIC_FILE)) if os.path.exists(TRAFFIC_FILE) else {}
+    sha = kernel_source_hash(weights)
+    for fn in sorted(glob.glob(os.path.join(csv_dir, "traffic_*.csv"))):
+        wl = os.path.basename(fn)[len("traffic_"):-len(".csv")]
+        rows = [r for r in csv.reader(open(fn)) if len(r) > 10]
+        hdr = rows[0]
+        ki, mi, vi, ids = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value", "ID"))
+        per = {}
+        for r in rows[1:]:
+            per.setdefault(r[ids], {"k": r[ki]})[r[mi]] = float(r[vi].replace(",", ""))
+        gu, dn = list(per.values())[:2]            # gate/up is launched before down
+        key = wl if weights == "bf16" else wl + "+" + weights
+        out[key] = {"source_sha256": sha, "kernel": gu["k"][:60],
+                    "bytes_per_launch": gu["dram__bytes_read.sum"] + gu["dram__bytes_write.sum"],
+                    "read": gu["dram__bytes_read.sum"], "write": gu["dram__bytes_write.sum"],
+                    "ns_under_ncu": gu["gpu__time_duration.sum"],
+                    "down_bytes_per_launch": dn["dram__bytes_read.sum"] + dn["dram__bytes_write.sum"]}
+    out["_comment"] = ("DRAM bytes per launch of the gate/up grouped GEMM (and of the down GEMM) from one-pass ncu "
+                       "captures; written by `python bench.py --write-traffic DIR`, see write_traffic().")
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(out, f, indent=1, sort_keys=True)
 
 
 def cpu_threads() -> int:
@@ -275,14 +323,28 @@ def run_ours(args, w):
                           n_shared=w.n_shared, score=w.score, renormalize=w.renormalize,
                           capacity_factor=w.capacity_factor, dtype=w.dtype)
     dev = synth.device_inputs(w)
+    fp8 = args.weights == "fp8"
+    if fp8:
+        # FP8 codes and per-row scales made on the device by the library's quantiser; the bf16
+        # copies are freed before any timing
+        for name in ("w_gate", "w_up", "w_down"):
+            dev[name + "_q"], dev[name + "_s"] = moe.moe_quantize_fp8_rows(dev[name])
+            del dev[name]
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        wargs = (dev["w_gate_q"], dev["w_gate_s"], dev["w_up_q"], dev["w_up_s"], dev["w_down_q"], dev["w_down_s"])
+        forward, forward_timed = moe.moe_layer_forward_fp8, moe.moe_layer_forward_fp8_timed
+    else:
+        wargs = (dev["w_gate"], dev["w_up"], dev["w_down"])
+        forward, forward_timed = moe.moe_layer_forward, moe.moe_layer_forward_timed
     ws = moe.alloc_workspace(cfg)
     dt = dev["x"].dtype
     out = torch.empty(w.T, w.d_model, dtype=dt, device="cuda")
     counts = torch.empty(w.n_experts, dtype=torch.int32, device="cuda")
-    args_fwd = (cfg, dev["x"], dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"], out, ws)
+    args_fwd = (cfg, dev["x"], dev["w_router"], dev["bias"], *wargs, out, ws)
 
     # one checked forward: status and the realised routing (kept pairs, experts touched)
-    moe.moe_layer_forward(*args_fwd, counts_out=counts)
+    forward(*args_fwd, counts_out=counts)
     status = moe.moe_get_device_error(ws)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status {moe.status_string(status)}")
@@ -290,7 +352,7 @@ def run_ours(args, w):
     c = counts.cpu().numpy()
     kept = int(np.minimum(c, cap).sum())
     touched = int((np.minimum(c, cap) > 0).sum()) + w.n_shared
-    work = algorithmic(w, kept, touched)
+    work = algorithmic(w, kept, touched, 1.0 if fp8 else 2.0)
 
     K, W = args.steps, args.warmup
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
@@ -298,14 +360,14 @@ def run_ours(args, w):
         for e in row:
             e.record()
     for i in range(W):
-        moe.moe_layer_forward_timed(*args_fwd, evs[i % K])
+        forward_timed(*args_fwd, evs[i % K])
     barrier()
     graph = None
     if not args.eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(K):
-                moe.moe_layer_forward_timed(*args_fwd, evs[i])
+                forward_timed(*args_fwd, evs[i])
         graph.replay()         # one untimed replay
         barrier()
     props = torch.cuda.get_device_properties(local)
@@ -323,7 +385,7 @@ def run_ours(args, w):
         graph.replay()
     else:
         for i in range(K):
-            moe.moe_layer_forward_timed(*args_fwd, evs[i])
+            forward_timed(*args_fwd, evs[i])
     t_end.record()
     barrier()
     clocks = sampler.stop()
@@ -343,11 +405,11 @@ def run_ours(args, w):
     x_host = dev["x"].cpu().pin_memory()
     out_host = torch.empty(out.shape, dtype=dt).pin_memory()
     x_dev = torch.empty_like(dev["x"])
-    args_e2e = (cfg, x_dev, dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"], out, ws)
+    args_e2e = (cfg, x_dev, dev["w_router"], dev["bias"], *wargs, out, ws)
     K2 = max(args.e2e_steps, 1)
     for _ in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(*args_e2e)
+        forward(*args_e2e)
         out_host.copy_(out, non_blocking=True)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -355,7 +417,7 @@ def run_ours(args, w):
     e0.record()
     for _ in range(K2):
         x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(*args_e2e)
+        forward(*args_e2e)
         out_host.copy_(out, non_blocking=True)
     e1.record()
     barrier()
@@ -380,8 +442,9 @@ def run_ours(args, w):
         achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.name)
-    roof["kernel"] = "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)"
+    roof["traffic"] = measured_traffic(w.name, args.weights)
+    roof["kernel"] = ("grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
+                      "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
     roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else f"{peak_src} copy bandwidth"
     roof["ms_per_launch"] = gemm_ms
 
@@ -408,7 +471,8 @@ def run_ours(args, w):
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step"
                          % (touched * 3.0 * w.d_model * w.d_ff * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": "eager" if args.eager else "cuda_graph"},
+                   "launch": "eager" if args.eager else "cuda_graph",
+                   "weights": "fp8 e4m3, per-row float32 scales" if fp8 else w.dtype},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
         "gpu_launches": K * moe.moe_layer_launch_count(cfg),
@@ -426,6 +490,9 @@ def run_ours(args, w):
 
 def main():
     args = parse_args()
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.weights)
+        return
     import synth
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -179,6 +179,37 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const 
                              void* y_perm, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * FP8 expert weights [ST "Memory vs compute, quantified": the 671B model's weights are about
+ * 671 GB in FP8 instead of 1.3 TB in BF16; small-batch decode streams the touched experts'
+ * weights, so their bytes set the step time]. A weight matrix is stored as E4M3 codes with one
+ * float32 scale per output row:  W[r][c] = scale[r] * e4m3(wq[r][c]).  For w_gate / w_up the
+ * rows are the d_ff outputs of each group ([G, d_ff, d_model] codes, [G, d_ff] scales); for
+ * w_down the d_model outputs ([G, d_model, d_ff] codes, [G, d_model] scales). Activations stay
+ * bf16; the kernels widen the codes to bf16 (exactly) in shared memory and apply the scales to
+ * the float32 accumulators, so a layer with FP8 weights computes exactly what the bf16 layer
+ * computes with the dequantized weights.
+ *
+ * Quantisation of a bf16 matrix [rows, cols] (cols a multiple of 16):
+ *   scale[r] = max_c |w[r][c]| / 448 (float32; 0 for an all-zero row)
+ *   wq[r][c] = E4M3 code of float32(w[r][c]) / scale[r], rounded to nearest even and saturated
+ *              to +-448 (0 when scale[r] = 0)
+ *   w   device [rows, cols] bf16 in;  wq device [rows, cols] uint8 out;  scale device [rows] float32 out
+ */
+moe_status_t moe_quantize_fp8_rows(const void* w, int64_t rows, int32_t cols, uint8_t* wq, float* scale,
+                                   cudaStream_t stream);
+
+/*
+ * moe_grouped_ffn with FP8 expert weights (bf16 layers only): the same rows and outputs as
+ * moe_grouped_ffn for the dequantized weights.
+ *   wg_q, wu_q  device [G, d_ff, d_model] uint8     wg_s, wu_s device [G, d_ff] float32
+ *   wd_q        device [G, d_model, d_ff] uint8     wd_s       device [G, d_model] float32
+ */
+moe_status_t moe_grouped_ffn_fp8(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                                 const void* x, const uint8_t* wg_q, const float* wg_s, const uint8_t* wu_q,
+                                 const float* wu_s, const uint8_t* wd_q, const float* wd_s, void* y_perm,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Combine [ST Q&A "How does a top-k router work?": gate-weighted sum of the selected experts;
  * ST "The router": shared experts every token visits; KG definition: undo the permutation]:
  *     out[t] = sum_{j: dest_row[t,j] >= 0} gate[t,j] * y_perm[dest_row[t,j]]  (+ y_perm[R + t] if S = 1)
@@ -240,6 +271,22 @@ typedef struct moe_routing_stats {
 
 moe_status_t moe_routing_stats(const moe_config_t* cfg, const int32_t* counts, moe_routing_stats_t* stats,
                                cudaStream_t stream);
+
+/*
+ * moe_layer_forward and moe_layer_forward_timed with FP8 expert weights (bf16 layers only; the
+ * weight arguments as for moe_grouped_ffn_fp8).
+ */
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const void* w_router,
+                                   const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                   const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                   const float* wd_s, void* out, int32_t* topk_idx_out, int32_t* counts_out,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream);
+moe_status_t moe_layer_forward_fp8_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                         const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                         const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                         const float* wd_s, void* out, int32_t* topk_idx_out,
+                                         int32_t* counts_out, void* ws, size_t ws_bytes,
+                                         void* const* events, int32_t n_events, cudaStream_t stream);
 
 /* Number of kernel launches one moe_layer_forward call enqueues for this configuration (-1 if invalid). */
 int32_t moe_layer_launch_count(const moe_config_t* cfg);

@@ -64,7 +64,7 @@ __all__ = [
     "router_logits", "scores_from_logits", "select_topk", "gates_from_scores", "route",
     "capacity", "dispatch", "silu", "expert_mlp", "combine", "layer_forward", "LayerResult",
     "flops_per_pair", "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
-    "routing_stats",
+    "routing_stats", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "dequantize_fp8_rows",
 ]
 
 
@@ -329,3 +329,63 @@ def routing_stats(counts, T: int, cap: Optional[int]) -> dict:
     return {"tokens": int(T), "pairs": int(c.sum()), "kept": K, "dropped": int(c.sum()) - K,
             "experts_touched": int((kept > 0).sum()), "max_load": M, "capacity": cap_v,
             "mean_load": mean, "efficiency": (mean / M) if M > 0 else Fraction(1)}
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) expert weights
+#
+# [ST "Memory vs compute, quantified": the 671B model's weights are about 671 GB in FP8.]
+# The pages name the format only; the encoding is the OCP 8-bit floating point E4M3 format:
+# 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0 holds the
+# subnormals m/8 * 2^-6; exponent 15 with mantissa 7 is NaN (no infinities); the largest
+# finite magnitude is 1.75 * 2^8 = 448. A weight row is stored as codes with one float32
+# scale: W[r][c] = scale[r] * value(code[r][c]).
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Exact float64 values of E4M3 codes."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """E4M3 code of each value: round to the nearest representable magnitude, ties to the even
+    mantissa code, magnitudes above 448 saturated to 448, the sign bit copied from the input
+    (so a negative value that rounds to zero gives negative zero, 0x80), NaN to 0x7F."""
+    x = np.asarray(v, dtype=np.float64)
+    codes = np.arange(0x7F, dtype=np.int64)                  # all non-negative finite codes
+    vals = e4m3_decode(codes)                                # increasing
+    mag = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(vals, mag, side="left"), 1, len(vals) - 1)
+    lo = hi - 1
+    d_lo = mag - vals[lo]
+    d_hi = vals[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes[hi] % 2 == 0))
+    code = np.where(pick_hi, codes[hi], codes[lo])
+    code = np.where(mag == vals[hi], codes[hi], code)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize_fp8_rows(w) -> tuple:
+    """Per-row E4M3 quantisation of float32-representable weights, in the arithmetic the codes
+    are defined with: scale = float32(max|w_row|) / float32(448) and code = E4M3 of
+    float32(w) / scale, both divisions rounded once to float32 (code 0 for an all-zero row).
+    Returns (codes uint8 [.., cols], scale float32 [..])."""
+    w32 = np.asarray(w, dtype=np.float32)
+    mx = np.max(np.abs(w32), axis=-1)
+    scale = (mx / np.float32(448.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    v = (w32 / safe[..., None]).astype(np.float32)
+    v = np.where(scale[..., None] > 0, v, np.float32(0.0))
+    return e4m3_encode(v), scale
+
+
+def dequantize_fp8_rows(codes, scale) -> np.ndarray:
+    """scale[r] * value(code[r][c]) in float64 (exact)."""
+    return np.asarray(scale, dtype=np.float64)[..., None] * e4m3_decode(codes)

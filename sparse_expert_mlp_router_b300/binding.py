@@ -23,7 +23,8 @@ EXPORTS = [
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
     "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
-    "moe_permute_noalloc", "moe_routing_stats",
+    "moe_permute_noalloc", "moe_routing_stats", "moe_quantize_fp8_rows", "moe_grouped_ffn_fp8",
+    "moe_layer_forward_fp8", "moe_layer_forward_fp8_timed",
 ]
 
 
@@ -96,6 +97,12 @@ def lib() -> ctypes.CDLL:
             "moe_layer_launch_count": ([_cfgp], i32),
             "moe_permute_noalloc": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
             "moe_routing_stats": ([_cfgp, _vp, _vp, _vp], i32),
+            "moe_quantize_fp8_rows": ([_vp, i64, i32, _vp, _vp, _vp], i32),
+            "moe_grouped_ffn_fp8": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz, _vp], i32),
+            "moe_layer_forward_fp8": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz,
+                                       _vp], i32),
+            "moe_layer_forward_fp8_timed": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                             _vp, sz, ctypes.POINTER(_vp), i32, _vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -250,3 +257,45 @@ def routing_stats_to_dict(stats) -> dict:
     raw = bytes(stats.cpu().numpy().tobytes())[:ctypes.sizeof(MoeRoutingStats)]
     st = MoeRoutingStats.from_buffer_copy(raw)
     return {n: getattr(st, n) for n in MoeRoutingStats.FIELDS}
+
+
+# ------------------------------------------------------------- FP8 weights
+
+def moe_quantize_fp8_rows(w, wq=None, scale=None, stream=None):
+    """E4M3 codes and per-row float32 scales of a bf16 matrix (any leading shape; rows are the
+    product of all but the last dimension). Returns (wq uint8, scale float32)."""
+    import torch
+    rows = w.numel() // w.shape[-1]
+    if wq is None:
+        wq = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    if scale is None:
+        scale = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(lib().moe_quantize_fp8_rows(_ptr(w), rows, w.shape[-1], _ptr(wq), _ptr(scale), _stream(stream)),
+           "moe_quantize_fp8_rows")
+    return wq, scale
+
+
+def moe_grouped_ffn_fp8(cfg, x_perm, offsets, x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, y_perm, ws, stream=None) -> None:
+    _check(lib().moe_grouped_ffn_fp8(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(x), _ptr(wg_q),
+                                     _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(y_perm),
+                                     _ptr(ws), ws.numel(), _stream(stream)), "moe_grouped_ffn_fp8")
+
+
+def moe_layer_forward_fp8(cfg, x, w_router, bias, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, out, ws, topk_idx_out=None,
+                          counts_out=None, stream=None) -> None:
+    _check(lib().moe_layer_forward_fp8(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(wg_q),
+                                       _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(out),
+                                       _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws), ws.numel(),
+                                       _stream(stream)), "moe_layer_forward_fp8")
+
+
+def moe_layer_forward_fp8_timed(cfg, x, w_router, bias, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, out, ws, events,
+                                topk_idx_out=None, counts_out=None, stream=None) -> None:
+    for e in events:
+        if e.cuda_event == 0:
+            e.record()
+    handles = (_vp * len(events))(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_fp8_timed(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(wg_q),
+                                             _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(out),
+                                             _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws), ws.numel(), handles,
+                                             len(events), _stream(stream)), "moe_layer_forward_fp8_timed")

@@ -1,0 +1,538 @@
+// Grouped expert GEMMs with FP8 (E4M3) expert weights and bf16 activations,
+// and the per-row quantiser that produces such weights.
+//
+// shubhamtatvamasi.com/llm-inference/moe "Mixture of Experts", section
+// "Memory vs compute, quantified": the weights of the 671B model are about
+// 671 GB in FP8 against 1.3 TB in BF16, and a decode step streams the touched
+// experts' weights, so halving their bytes halves the memory-bound part of the
+// step. The contraction is the one of gemm_tc.cu (the SwiGLU expert of
+// klaylearn.com's "Mixture of Experts" grouped GEMMs) with each weight row
+// scaled: W[r][:] = scale[r] * e4m3(wq[r][:]).
+//
+// Every E4M3 value is exactly a bf16 value, and a per-output-row scale factors
+// out of the dot product, so the tensor cores run kind::f16 on bf16 operands:
+//   warp 0       TMA producer of the bf16 A tiles (128 x 64) into a 3-stage ring
+//   warp 1       MMA issuer (tcgen05 M=128, N=256, K=16), two TMEM accumulators
+//   warp 2       TMA producer of the weight codes (256 rows x 64 bytes per k-step)
+//                into a 4-slot staging ring, so more DRAM bytes are in flight
+//                than the bf16 stages alone would allow
+//   warps 3-6    epilogue: per-column scales applied to the float32 accumulator
+//                (before the SwiGLU for gate/up), bf16 stores of the valid rows
+//   warps 7-14   widen the codes to bf16 into the stage's B region in the
+//                128-byte-swizzled K-major layout the MMA reads (the pattern a
+//                TMA SWIZZLE_128B load writes: 16-byte chunk c of row r at chunk
+//                c ^ (r mod 8)), then a proxy fence and an arrive hand the tile
+//                to the tensor cores
+// Tiles, schedule and bounded waits are those of the bf16 single-CTA kernel.
+#include <cuda_fp8.h>
+
+#include "gemm_common.cuh"
+#include "internal.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
+
+namespace moe {
+namespace {
+
+using gemm::decode_tile;
+using gemm::drain_fills;
+using gemm::kDrainLimitNs;
+using gemm::kWaitLimitNs;
+using gemm::pack_bf16;
+using gemm::silu_f;
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 3;                       // A + widened B per stage
+constexpr int kQStages = 4;                      // weight codes per slot
+constexpr int kABytes = kBM * kBK * 2;           // 16 KB
+constexpr int kBRows = 256;                      // gate/up: 128 W_gate + 128 W_up rows; down: 256 W_down rows
+constexpr int kBBytes = kBRows * kBK * 2;        // 32 KB of bf16
+constexpr int kQBytes = kBRows * kBK;            // 16 KB of codes
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 4;
+constexpr int kConvWarps = 8;
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kFirstEpiWarp = 3;
+constexpr int kFirstConvWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 480
+constexpr int kSchedInts = 4 * (kMaxExperts + 2);
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kQStages * kQBytes + 512 /*barriers*/ +
+                         256 * 4 /*column scales*/ + (size_t)kSchedInts * 4;
+
+struct Fp8Args {
+  int K;                 // reduction length
+  int n_tiles;           // N tiles per group
+  int G;                 // groups
+  int shared_from;       // groups >= shared_from read A from the second A map (gate/up only)
+  int b_rows;            // weight rows per group (F for gate/up, d for down)
+  const int32_t* sched;  // device group schedule
+  const float* scale;    // gate/up: W_gate row scales [G, F]; down: W_down row scales [G, d]
+  const float* scale2;   // gate/up: W_up row scales [G, F]
+  __nv_bfloat16* out;
+  int64_t ldo;
+  int32_t* status;
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory"); }
+
+// Two E4M3 codes (low byte first) -> bf16x2 (exact).
+__device__ __forceinline__ uint32_t widen2(uint32_t pair) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_bfloat162 b = __float22bfloat162_rn(f);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQ2,
+                         const Fp8Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);   // 1024-byte aligned
+  uint8_t* stage_base = smem;
+  uint8_t* code_base = smem + (size_t)kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(code_base + (size_t)kQStages * kQBytes);
+  uint64_t* full = bars;                       // [kStages] A landed
+  uint64_t* conv = full + kStages;             // [kStages] B widened
+  uint64_t* empty = conv + kStages;            // [kStages] stage read by the MMAs
+  uint64_t* qfull = empty + kStages;           // [kQStages] codes landed
+  uint64_t* qempty = qfull + kQStages;         // [kQStages] codes read by the converters
+  uint64_t* tfull = qempty + kQStages;         // [2]
+  uint64_t* tempty = tfull + 2;                // [2]
+  uint64_t* drain = tempty + 2;                // [1]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* s_stop = reinterpret_cast<volatile int*>(tmem_holder + 2);   // epilogue's snapshot
+  float* s_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);   // [256]
+  int32_t* s_tile_start = reinterpret_cast<int32_t*>(s_scale + 256);
+  int32_t* s_a_row = s_tile_start + (args.G + 1);
+  int32_t* s_out_row = s_a_row + args.G;
+  int32_t* s_rows = s_out_row + args.G;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i < 4 * args.G + 1; i += kThreads) s_tile_start[i] = args.sched[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&conv[s]), kConvThreads);
+      ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
+    }
+    for (int q = 0; q < kQStages; ++q) {
+      ptx::mbar_init(ptx::smem_u32(&qfull[q]), 1);
+      ptx::mbar_init(ptx::smem_u32(&qempty[q]), kConvThreads);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(ptx::smem_u32(&tfull[a]), 1);
+      ptx::mbar_init(ptx::smem_u32(&tempty[a]), 32 * kEpiWarps);
+    }
+    ptx::mbar_init(ptx::smem_u32(drain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    if (MODE == 0) ptx::prefetch_tmap(&tmA2);
+  }
+  if (warp == 2 && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    if (MODE == 0) ptx::prefetch_tmap(&tmQ2);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_holder), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int total_tiles = s_tile_start[args.G] * args.n_tiles;
+  const int k_steps = args.K / kBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ A producer
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
+        int g, m, n;
+        decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
+        const bool use_a2 = (MODE == 0) && (g >= args.shared_from);
+        const int a_row = ((MODE == 0) ? s_a_row[g] : s_out_row[g]) + m * kBM;
+        for (int kb = 0; kb < k_steps; ++kb) {
+          if (!ptx::mbar_wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_u32(&full[stage]);
+          ptx::mbar_arrive_expect_tx(fb, kABytes);
+          ptx::tma_load_2d(ptx::smem_u32(stage_base + (size_t)stage * kStageBytes),
+                           use_a2 ? (const void*)&tmA2 : (const void*)&tmA, kb * kBK, a_row, fb);
+          if (issued < kStages) ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        drain_fills(full, kStages, stage, phase, issued);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ weight-code producer
+    if (lane == 0) {
+      int slot = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
+        int g, m, n;
+        decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
+        const int b_row = g * args.b_rows + n * ((MODE == 0) ? 128 : 256);
+        for (int kb = 0; kb < k_steps; ++kb) {
+          if (!ptx::mbar_wait_bounded(ptx::smem_u32(&qempty[slot]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = ptx::smem_u32(&qfull[slot]);
+          const uint32_t dst = ptx::smem_u32(code_base + (size_t)slot * kQBytes);
+          ptx::mbar_arrive_expect_tx(fb, kQBytes);
+          if (MODE == 0) {
+            ptx::tma_load_2d(dst, &tmQ, kb * kBK, b_row, fb);              // W_gate codes
+            ptx::tma_load_2d(dst + 128 * kBK, &tmQ2, kb * kBK, b_row, fb); // W_up codes
+          } else {
+            ptx::tma_load_2d(dst, &tmQ, kb * kBK, b_row, fb);
+            ptx::tma_load_2d(dst + 128 * kBK, &tmQ, kb * kBK, b_row + 128, fb);
+          }
+          if (issued < kQStages) ++issued;
+          if (++slot == kQStages) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        drain_fills(qfull, kQStages, slot, phase, issued);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, 256);
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        for (int kb = 0; kb < k_steps; ++kb) {
+          if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
+              !ptx::mbar_wait_bounded(ptx::smem_u32(&conv[stage]), phase, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(stage_base + (size_t)stage * kStageBytes);
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(sa);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(sa + kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            ptx::mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+          ptx::mma_commit(ptx::smem_u32(&empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(ptx::smem_u32(&tfull[acc]));
+      }
+      if (!ok) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      ptx::mma_commit(ptx::smem_u32(drain));
+      ptx::mbar_wait_bounded(ptx::smem_u32(drain), 0, nullptr, kDrainLimitNs);
+    }
+  } else if (warp < kFirstConvWarp) {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 32 * kFirstEpiWarp;        // 0..127
+    const int quarter = warp & 3;
+    const int r_local = quarter * 32 + lane;
+    int it = 0;
+    for (int L = blockIdx.x; L < total_tiles; L += gridDim.x, ++it) {
+      int g, m, n;
+      decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      if (!ptx::mbar_wait_bounded(ptx::smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs)) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // The tile's column scales, shared by the four warps. Every epilogue thread passes both
+      // barriers, and all of them leave on the same snapshot of the abort flag (taken between
+      // the barriers), so no warp is left waiting at a barrier the others have left.
+      epi_bar();
+      if (et == 0) *s_stop = *abort_flag;
+      if (MODE == 0) {
+        s_scale[et] = args.scale[(size_t)g * args.b_rows + n * 128 + et];
+        s_scale[128 + et] = args.scale2[(size_t)g * args.b_rows + n * 128 + et];
+      } else {
+        s_scale[et] = args.scale[(size_t)g * args.b_rows + n * 256 + et];
+        s_scale[128 + et] = args.scale[(size_t)g * args.b_rows + n * 256 + 128 + et];
+      }
+      epi_bar();
+      if (*s_stop != 0) break;
+      ptx::tc_fence_after();
+      const bool valid = (m * kBM + r_local) < s_rows[g];
+      const int64_t out_row = (int64_t)s_out_row[g] + m * kBM + r_local;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256);
+      if (MODE == 0) {
+        __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gv[32], uv[32];
+          ptx::tmem_ld32(t_row + c, gv);
+          ptx::tmem_ld32(t_row + 128 + c, uv);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float g0 = __uint_as_float(gv[2 * q]) * s_scale[c + 2 * q];
+              const float g1 = __uint_as_float(gv[2 * q + 1]) * s_scale[c + 2 * q + 1];
+              const float u0 = __uint_as_float(uv[2 * q]) * s_scale[128 + c + 2 * q];
+              const float u1 = __uint_as_float(uv[2 * q + 1]) * s_scale[128 + c + 2 * q + 1];
+              packed[q] = pack_bf16(silu_f(g0) * u0, silu_f(g1) * u1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 256;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + c, v);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              packed[q] = pack_bf16(__uint_as_float(v[2 * q]) * s_scale[c + 2 * q],
+                                    __uint_as_float(v[2 * q + 1]) * s_scale[c + 2 * q + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&tempty[acc]));
+    }
+  } else {
+    // ------------------------------------------------------------ code widening
+    const int ct = threadIdx.x - 32 * kFirstConvWarp;       // 0..255
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, qphase = 0;
+    for (int L = blockIdx.x; L < total_tiles; L += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < k_steps; ++kb) {
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&qfull[slot]), qphase, abort_flag, kWaitLimitNs) ||
+            !ptx::mbar_wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* codes = code_base + (size_t)slot * kQBytes;
+        uint8_t* bdst = stage_base + (size_t)stage * kStageBytes + kABytes;
+#pragma unroll
+        for (int u = 0; u < (kBRows * 4) / kConvThreads; ++u) {
+          const int t = ct + u * kConvThreads;
+          const int r = t >> 2, j = t & 3;                    // row, 16-code group
+          const uint4 raw = *reinterpret_cast<const uint4*>(codes + r * kBK + j * 16);
+          const uint4 lo = make_uint4(widen2(raw.x), widen2(raw.x >> 16), widen2(raw.y), widen2(raw.y >> 16));
+          const uint4 hi = make_uint4(widen2(raw.z), widen2(raw.z >> 16), widen2(raw.w), widen2(raw.w >> 16));
+          uint8_t* rowp = bdst + (r >> 3) * 1024 + (r & 7) * 128;
+          *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();                            // widened tile visible to the MMA
+        ptx::mbar_arrive(ptx::smem_u32(&conv[stage]));
+        ptx::mbar_arrive(ptx::smem_u32(&qempty[slot]));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++slot == kQStages) {
+          slot = 0;
+          qphase ^= 1u;
+        }
+      }
+      if (!ok) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// One warp per row: the row's absolute maximum, its scale, then the codes, 16 per lane step.
+__global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ w, int64_t rows, int cols,
+                                         uint8_t* __restrict__ wq, float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const __nv_bfloat16* src = w + r * cols;
+    float mx = 0.0f;
+    for (int c = lane * 8; c < cols; c += 256) {
+      const uint4 u = *reinterpret_cast<const uint4*>(src + c);
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mx = fmaxf(mx, fabsf(__uint_as_float(wd[i] << 16)));
+        mx = fmaxf(mx, fabsf(__uint_as_float(wd[i] & 0xFFFF0000u)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float s = __fdiv_rn(mx, 448.0f);
+    if (lane == 0) scale[r] = s;
+    for (int c = lane * 16; c < cols; c += 512) {
+      const uint4 a = *reinterpret_cast<const uint4*>(src + c);
+      const uint4 b = *reinterpret_cast<const uint4*>(src + c + 8);
+      const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t pair = wd[2 * i + h];
+          float2 v = make_float2(__uint_as_float(pair << 16), __uint_as_float(pair & 0xFFFF0000u));
+          if (s > 0.0f) {
+            v.x = __fdiv_rn(v.x, s);
+            v.y = __fdiv_rn(v.y, s);
+          } else {
+            v = make_float2(0.0f, 0.0f);
+          }
+          const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+          word |= (uint32_t)q << (16 * h);
+        }
+        out[i] = word;
+      }
+      *reinterpret_cast<uint4*>(wq + r * cols + c) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+  }
+}
+
+template <int MODE>
+cudaError_t launch_fp8w(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& q, const CUtensorMap& q2,
+                        const Fp8Args& args, int64_t max_tiles, cudaStream_t st) {
+  auto kern = grouped_gemm_fp8w_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e != cudaSuccess) return e;
+  int64_t grid = num_sms();
+  if (max_tiles < grid) grid = max_tiles;
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, kSmem, st>>>(a, a2, q, q2, args);
+  return cudaGetLastError();
+}
+
+int64_t max_m_tiles(const Shape& s) {
+  return (s.R + kBM - 1) / kBM + s.E + (int64_t)s.S * ((s.T + kBM - 1) / kBM);
+}
+
+}  // namespace
+
+bool fp8w_supported(const Shape& s) { return s.dtype == MOE_BF16 && s.d % 256 == 0 && s.F % 128 == 0; }
+
+cudaError_t launch_quantize_fp8_rows(const void* w, int64_t rows, int cols, uint8_t* wq, float* scale,
+                                     cudaStream_t st) {
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quantize_fp8_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w), rows, cols, wq,
+                                                             scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const void* x, const uint8_t* wg_q,
+                                    const float* wg_s, const uint8_t* wu_q, const float* wu_s, const void* sched,
+                                    void* h, int32_t* status, cudaStream_t st) {
+  CUtensorMap a, a2, q, q2;
+  const uint64_t R = (uint64_t)(s.R > 0 ? s.R : 1);
+  if (!make_tmap_bf16(&a, x_perm, s.d, R, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&a2, s.S > 0 ? x : x_perm, s.d, s.S > 0 ? (uint64_t)s.T : R, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&q, wg_q, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&q2, wu_q, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
+  Fp8Args args{};
+  args.K = s.d;
+  args.n_tiles = s.F / 128;
+  args.G = s.G;
+  args.shared_from = s.E;
+  args.b_rows = s.F;
+  args.sched = static_cast<const int32_t*>(sched);
+  args.scale = wg_s;
+  args.scale2 = wu_s;
+  args.out = static_cast<__nv_bfloat16*>(h);
+  args.ldo = s.F;
+  args.status = status;
+  return launch_fp8w<0>(a, a2, q, q2, args, max_m_tiles(s) * args.n_tiles, st);
+}
+
+cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* wd_q, const float* wd_s,
+                                  const void* sched, void* y, int32_t* status, cudaStream_t st) {
+  CUtensorMap a, q;
+  const uint64_t rows = (uint64_t)s.R + (uint64_t)s.S * s.T;
+  if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&q, wd_q, s.F, (uint64_t)s.G * s.d, 128)) return cudaErrorInvalidValue;
+  Fp8Args args{};
+  args.K = s.F;
+  args.n_tiles = s.d / 256;
+  args.G = s.G;
+  args.shared_from = s.G;
+  args.b_rows = s.d;
+  args.sched = static_cast<const int32_t*>(sched);
+  args.scale = wd_s;
+  args.scale2 = wd_s;
+  args.out = static_cast<__nv_bfloat16*>(y);
+  args.ldo = s.d;
+  args.status = status;
+  return launch_fp8w<1>(a, a, q, q, args, max_m_tiles(s) * args.n_tiles, st);
+}
+
+}  // namespace moe

@@ -57,6 +57,7 @@
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace {
@@ -65,8 +66,12 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;              // one 128-byte swizzle atom of bf16
 constexpr int kEpiWarps = 8;         // two per 32-lane TMEM quarter
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;     // 4 s: far beyond any legitimate wait
-constexpr uint64_t kDrainLimitNs = 100000000ull;     // 100 ms for draining after an abort
+using gemm::kWaitLimitNs;
+using gemm::kDrainLimitNs;
+using gemm::decode_tile;
+using gemm::silu_f;
+using gemm::pack_bf16;
+using gemm::drain_fills;
 constexpr int kSchedInts = 5 * (kMaxExperts + 2);    // schedule + a tile prefix, in shared memory
 
 struct GemmArgs {
@@ -80,28 +85,6 @@ struct GemmArgs {
   int64_t ldo;          // elements per output row
   int32_t* status;
 };
-
-// Tiles ordered (group, n-tile, m-tile) from a prefix of m-tiles per group.
-__device__ __forceinline__ void decode_tile(int L, const int32_t* tile_start, int G, int nt, int& g, int& m,
-                                            int& n) {
-  int lo = 0, hi = G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_start[mid] * nt <= L) lo = mid; else hi = mid;
-  }
-  g = lo;
-  const int mt = tile_start[g + 1] - tile_start[g];
-  const int local = L - tile_start[g] * nt;
-  n = local / mt;
-  m = local - n * mt;
-}
-
-__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // Epilogue of one accumulator row (this thread's TMEM lane): output columns
 // [half * COLS/2, (half + 1) * COLS/2) of the tile, written at `orow`. MODE 0 reads gate
@@ -146,20 +129,6 @@ __device__ __forceinline__ void store_tile(uint32_t t_row, bool valid, __nv_bflo
           dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       }
     }
-  }
-}
-
-// After an abort: the most recent fill of each of the `issued` slots before (stage, phase)
-// lands before the shared memory is left. A fill whose phase already completed passes at once.
-__device__ __forceinline__ void drain_fills(uint64_t* full, int n_stages, int stage, uint32_t phase, int issued) {
-  for (int j = 0; j < issued; ++j) {
-    if (stage == 0) {
-      stage = n_stages - 1;
-      phase ^= 1u;
-    } else {
-      --stage;
-    }
-    ptx::mbar_wait_bounded(ptx::smem_u32(&full[stage]), phase, nullptr, kDrainLimitNs);
   }
 }
 

@@ -106,6 +106,16 @@ cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void
 cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_down,
                                 const void* sched, void* y, int32_t* status, cudaStream_t st);
 
+// FP8 (E4M3) expert weights with per-row float32 scales (gemm_fp8w.cu).
+bool fp8w_supported(const Shape& s);
+cudaError_t launch_quantize_fp8_rows(const void* w, int64_t rows, int cols, uint8_t* wq, float* scale,
+                                     cudaStream_t st);
+cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const void* x, const uint8_t* wg_q,
+                                    const float* wg_s, const uint8_t* wu_q, const float* wu_s, const void* sched,
+                                    void* h, int32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* wd_q, const float* wd_s,
+                                  const void* sched, void* y, int32_t* status, cudaStream_t st);
+
 cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_row,
                            const float* gate, void* out, int32_t* status, cudaStream_t st);
 

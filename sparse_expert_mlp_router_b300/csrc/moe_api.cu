@@ -172,19 +172,48 @@ cudaError_t run_schedule(const Shape& s, const WsLayout& L, void* ws, const int3
   return launch_group_schedule(s, offsets, at<void>(ws, L.sched), at<int32_t>(ws, L.status), st);
 }
 
-cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const void* x, const void* wg,
-                    const void* wu, const void* wd, void* y, cudaStream_t st, cudaEvent_t mid_event) {
+// Expert weights of a call: bf16 / float32 tensors, or FP8 codes with per-row scales.
+struct ExpertWeights {
+  const void* g;
+  const void* u;
+  const void* d;
+  const float* gs = nullptr;
+  const float* us = nullptr;
+  const float* ds = nullptr;
+  bool fp8 = false;
+};
+
+cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const void* x,
+                    const ExpertWeights& w, void* y, cudaStream_t st, cudaEvent_t mid_event) {
   int32_t* status = at<int32_t>(ws, L.status);
   void* sched = at<void>(ws, L.sched);
   void* h = at<void>(ws, L.h);
   cudaError_t e;
-  if (s.dtype == MOE_BF16) {
-    if ((e = launch_gemm_gateup_tc(s, x_perm, x, wg, wu, sched, h, status, st)) != cudaSuccess) return e;
+  if (w.fp8) {
+    if ((e = launch_gemm_gateup_fp8w(s, x_perm, x, static_cast<const uint8_t*>(w.g), w.gs,
+                                     static_cast<const uint8_t*>(w.u), w.us, sched, h, status, st)) != cudaSuccess)
+      return e;
     if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
-    return launch_gemm_down_tc(s, h, wd, sched, y, status, st);
+    return launch_gemm_down_fp8w(s, h, static_cast<const uint8_t*>(w.d), w.ds, sched, y, status, st);
+  }
+  if (s.dtype == MOE_BF16) {
+    if ((e = launch_gemm_gateup_tc(s, x_perm, x, w.g, w.u, sched, h, status, st)) != cudaSuccess) return e;
+    if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
+    return launch_gemm_down_tc(s, h, w.d, sched, y, status, st);
   }
   if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
-  return launch_ffn_fma(s, x_perm, x, wg, wu, wd, sched, h, y, st);
+  return launch_ffn_fma(s, x_perm, x, w.g, w.u, w.d, sched, h, y, st);
+}
+
+// FP8 weights: bf16 layers whose shapes the FP8 kernels take, aligned codes and scales.
+moe_status_t check_fp8_weights(const Shape& s, const uint8_t* wg_q, const float* wg_s, const uint8_t* wu_q,
+                               const float* wu_s, const uint8_t* wd_q, const float* wd_s) {
+  if (!wg_q || !wg_s || !wu_q || !wu_s || !wd_q || !wd_s) return MOE_ERR_INVALID_ARG;
+  if (!aligned(wg_q, 16) || !aligned(wu_q, 16) || !aligned(wd_q, 16) || !aligned(wg_s, 4) || !aligned(wu_s, 4) ||
+      !aligned(wd_s, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (!fp8w_supported(s)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
 }
 
 // Kernel launches one moe_layer_forward enqueues.
@@ -196,18 +225,20 @@ int layer_launches(const Shape& s) {
 }
 
 moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
-                           const void* w_gate, const void* w_up, const void* w_down, void* out,
-                           int32_t* topk_idx_out, int32_t* counts_out, void* ws, size_t ws_bytes,
-                           void* const* events, int n_events, cudaStream_t st) {
+                           const ExpertWeights& w, void* out, int32_t* topk_idx_out, int32_t* counts_out, void* ws,
+                           size_t ws_bytes, void* const* events, int n_events, cudaStream_t st) {
   moe_status_t rc = check_cfg(cfg);
   if (rc != MOE_OK) return rc;
-  if (!x || !w_router || !w_gate || !w_up || !w_down || !out) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
-      !aligned(w_down, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4)) ||
+  if (!x || !w_router || !w.g || !w.u || !w.d || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(w.g, 16) || !aligned(w.u, 16) ||
+      !aligned(w.d, 16) || !aligned(out, 16) || (bias && !aligned(bias, 4)) ||
       (topk_idx_out && !aligned(topk_idx_out, 4)) || (counts_out && !aligned(counts_out, 4)))
     return MOE_ERR_INVALID_ARG;
   if (n_events < 0 || n_events > 6 || (n_events > 0 && events == nullptr)) return MOE_ERR_INVALID_ARG;
   const Shape s = make_shape(*cfg);
+  if (w.fp8 && (rc = check_fp8_weights(s, static_cast<const uint8_t*>(w.g), w.gs, static_cast<const uint8_t*>(w.u),
+                                       w.us, static_cast<const uint8_t*>(w.d), w.ds)) != MOE_OK)
+    return rc;
   if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
   const WsLayout L = make_layout(s);
   cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -230,7 +261,7 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark(2)) return MOE_ERR_CUDA;
-  if (run_ffn(s, L, ws, x_perm, x, w_gate, w_up, w_down, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
+  if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(4)) return MOE_ERR_CUDA;
   if (launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(5)) return MOE_ERR_CUDA;
@@ -337,7 +368,8 @@ moe_status_t moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const 
   const WsLayout L = make_layout(s);
   cudaError_t e = run_schedule(s, L, ws, offsets, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(run_ffn(s, L, ws, x_perm, x ? x : x_perm, w_gate, w_up, w_down, y_perm, stream, nullptr));
+  return cuda_status(run_ffn(s, L, ws, x_perm, x ? x : x_perm, ExpertWeights{w_gate, w_up, w_down}, y_perm, stream,
+                             nullptr));
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* dest_row,
@@ -357,16 +389,60 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const void* x, const voi
                                const void* w_gate, const void* w_up, const void* w_down, void* out,
                                int32_t* topk_idx_out, int32_t* counts_out, void* ws, size_t ws_bytes,
                                cudaStream_t stream) {
-  return layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, topk_idx_out, counts_out, ws, ws_bytes,
-                       nullptr, 0, stream);
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{w_gate, w_up, w_down}, out, topk_idx_out, counts_out,
+                       ws, ws_bytes, nullptr, 0, stream);
+}
+
+moe_status_t moe_layer_forward_fp8(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                                   const uint8_t* wg_q, const float* wg_s, const uint8_t* wu_q, const float* wu_s,
+                                   const uint8_t* wd_q, const float* wd_s, void* out, int32_t* topk_idx_out,
+                                   int32_t* counts_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true}, out,
+                       topk_idx_out, counts_out, ws, ws_bytes, nullptr, 0, stream);
+}
+
+moe_status_t moe_layer_forward_fp8_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                         const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                         const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                         const float* wd_s, void* out, int32_t* topk_idx_out, int32_t* counts_out,
+                                         void* ws, size_t ws_bytes, void* const* events, int32_t n_events,
+                                         cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true}, out,
+                       topk_idx_out, counts_out, ws, ws_bytes, events, n_events, stream);
+}
+
+moe_status_t moe_grouped_ffn_fp8(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets, const void* x,
+                                 const uint8_t* wg_q, const float* wg_s, const uint8_t* wu_q, const float* wu_s,
+                                 const uint8_t* wd_q, const float* wd_s, void* y_perm, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  moe_status_t rc = check_cfg(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!x_perm || !offsets || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && !x) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_perm, 16) || !aligned(offsets, 4) || (x && !aligned(x, 16)) || !aligned(y_perm, 16))
+    return MOE_ERR_INVALID_ARG;
+  const Shape s = make_shape(*cfg);
+  if ((rc = check_fp8_weights(s, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s)) != MOE_OK) return rc;
+  if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
+  const WsLayout L = make_layout(s);
+  if (run_schedule(s, L, ws, offsets, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(run_ffn(s, L, ws, x_perm, x ? x : x_perm,
+                             ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true}, y_perm, stream, nullptr));
+}
+
+moe_status_t moe_quantize_fp8_rows(const void* w, int64_t rows, int32_t cols, uint8_t* wq, float* scale,
+                                   cudaStream_t stream) {
+  if (!w || !wq || !scale || rows < 1 || cols < 16 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(scale, 4)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_fp8_rows(w, rows, cols, wq, scale, stream));
 }
 
 moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, const void* w_router,
                                      const float* bias, const void* w_gate, const void* w_up, const void* w_down,
                                      void* out, int32_t* topk_idx_out, int32_t* counts_out, void* ws,
                                      size_t ws_bytes, void* const* events, int32_t n_events, cudaStream_t stream) {
-  return layer_forward(cfg, x, w_router, bias, w_gate, w_up, w_down, out, topk_idx_out, counts_out, ws, ws_bytes,
-                       events, n_events, stream);
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{w_gate, w_up, w_down}, out, topk_idx_out, counts_out,
+                       ws, ws_bytes, events, n_events, stream);
 }
 
 int32_t moe_layer_launch_count(const moe_config_t* cfg) {

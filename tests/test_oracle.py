@@ -382,3 +382,42 @@ def test_routing_stats_agree_with_dispatch():
     assert st["dropped"] == int((d.dest_row < 0).sum())
     assert st["experts_touched"] == O.experts_touched(idx[d.dest_row >= 0], E)
     assert st["max_load"] <= cap
+
+
+# ------------------------------------------------------------ FP8 weights ---
+
+def test_e4m3_codes_from_the_format():
+    vals = O.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert np.isnan(vals[0x7F]) and np.isnan(vals[0xFF]) and np.isfinite(np.delete(vals, [0x7F, 0xFF])).all()
+    assert vals[0x7E] == 448.0 and vals[0x01] == 2.0 ** -9 and vals[0x08] == 2.0 ** -6 and vals[0x38] == 1.0
+    assert vals[0x80] == 0.0 and np.signbit(vals[0x80]) and vals[0xC0] == -2.0
+    finite = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    assert (O.e4m3_encode(vals[finite]) == np.array(finite, dtype=np.uint8)).all()      # round trip
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    vals = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2                     # exact midpoints between neighbours
+    got = O.e4m3_encode(mids)
+    want = np.where(np.arange(0x7E) % 2 == 0, np.arange(0x7E), np.arange(1, 0x7F))
+    assert (got == want).all()                            # ties go to the even code
+    assert (O.e4m3_encode(mids * (1 + 1e-9)) == np.arange(1, 0x7F)).all()
+    assert O.e4m3_encode([1e6, -1e6, 449.0])[0] == 0x7E and O.e4m3_encode([-1e6])[0] == 0xFE
+    assert O.e4m3_encode([-1e-30])[0] == 0x80 and np.isnan(O.e4m3_decode(O.e4m3_encode([np.nan])))[0]
+
+
+def test_quantize_rows_error_bound_and_scale():
+    rng = _rng(3)
+    w = (rng.standard_normal((40, 96)) * 0.02).astype(np.float32)
+    w[5] = 0.0
+    q, s = O.quantize_fp8_rows(w)
+    assert s.dtype == np.float32 and s[5] == 0 and (q[5] == 0).all()
+    deq = O.dequantize_fp8_rows(q, s)
+    rows = np.arange(40) != 5
+    # the largest magnitude of a row lands on +-448 (within the float32 rounding of the scale)
+    top = np.abs(w[rows]).argmax(axis=1)
+    assert np.all(np.abs(O.e4m3_decode(q[rows][np.arange(39), top])) == 448.0)
+    # every element within half a mantissa step (2^-4 relative) or half the subnormal step
+    err = np.abs(deq[rows] - w[rows].astype(np.float64))
+    bound = np.maximum(np.abs(w[rows]) * 2.0 ** -4, s[rows, None] * 2.0 ** -10) * (1 + 1e-6)
+    assert (err <= bound).all()
