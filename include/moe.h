@@ -199,8 +199,9 @@ moe_status_t moe_quantize_fp8_rows(const void* w, int64_t rows, int32_t cols, ui
                                    cudaStream_t stream);
 
 /*
- * moe_grouped_ffn with FP8 expert weights (bf16 layers only): the same rows and outputs as
- * moe_grouped_ffn for the dequantized weights.
+ * moe_grouped_ffn with FP8 expert weights: the same rows and outputs as moe_grouped_ffn for the
+ * dequantized weights. bf16 layers with d_model a multiple of 256 only; MOE_ERR_UNSUPPORTED
+ * otherwise (float32 activations, or d_model = 128 mod 256).
  *   wg_q, wu_q  device [G, d_ff, d_model] uint8     wg_s, wu_s device [G, d_ff] float32
  *   wd_q        device [G, d_model, d_ff] uint8     wd_s       device [G, d_model] float32
  */

@@ -41,9 +41,22 @@ def _quantized(dev, w):
     return out
 
 
-@pytest.mark.parametrize("name", ["mini_qwen3", "mini_deepseek", "mini_mixtral", "mini_decode"])
+LAYER_CASES = {
+    "mini_qwen3": ("mini_qwen3", {}),
+    "mini_deepseek": ("mini_deepseek", {}),
+    "mini_mixtral": ("mini_mixtral", {}),
+    "mini_decode": ("mini_decode", {}),
+    # d_ff of 384: three 128-feature gate/up tiles, a down-GEMM reduction of six 64-wide k-steps
+    "f384": ("mini_qwen3", {"d_ff": 384}),
+    # ~2400 kept pairs over 8 skewed experts: the largest expert spans ten 128-row tiles, the last ragged
+    "many_blocks": ("mini_mixtral", {"T": 1200}),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
 def test_layer_fp8_matches_oracle(name):
-    w = synth.WORKLOADS[name]
+    base, over = LAYER_CASES[name]
+    w = synth.WORKLOADS[base].with_(**over) if over else synth.WORKLOADS[base]
     inp = Inputs(w)
     dev = inp.device()
     cfg = cfg_of(w)
@@ -140,3 +153,62 @@ def test_fp8_refuses_shapes_it_does_not_take():
         moe.moe_layer_forward_fp8(cfg, dev["x"], dev["w_router"], dev["bias"], *q["w_gate"], *q["w_up"],
                                   *q["w_down"], out, ws)
     assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_fp8_refuses_float32_activations():
+    w = synth.WORKLOADS["tiny_f32"]
+    cfg = cfg_of(w)
+    dev = Inputs(w).device()
+    q = {n: moe.moe_quantize_fp8_rows(dev[n].to(torch.bfloat16)) for n in ("w_gate", "w_up", "w_down")}
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty(w.T, w.d_model, dtype=torch.float32, device="cuda")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_layer_forward_fp8(cfg, dev["x"], dev["w_router"], dev["bias"], *q["w_gate"], *q["w_up"],
+                                  *q["w_down"], out, ws)
+    assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T", [256, 32])
+@pytest.mark.parametrize("which", ["gate", "up", "down"])
+def test_every_e4m3_code_widens_exactly(which, T):
+    """Hand-made codes at scale 1 through moe_grouped_ffn_fp8, all tokens in expert 0.
+
+    Token t is the unit vector e_t and the matrices not under test are all-ones or the identity
+    (code 0x38 = 1.0), so every output is one decoded code through one SwiGLU:
+      gate  y[t,j] = silu(dec(c[j,t]))            (W_up all ones, W_down the identity)
+      up    y[t,j] = silu(1) * dec(c[j,t])        (W_gate all ones, W_down the identity)
+      down  y[t,j] = bf16(silu(1)) * dec(c[j,t])  (W_gate all ones, W_up the identity)
+    with c[j,t] = (j + t) mod 256 sweeping every code but the two NaNs over j for each token (T=256:
+    two 128-row token tiles; T=32: one ragged tile). A wrongly widened code
+    (subnormals, -0, the +-448 ends) shows as a relative error of that single output. Bound:
+    one bf16 rounding of y (2^-9), the bf16 rounding of h = silu(1) in the down case (8.1e-4)
+    and float32 silu; 2^-7 covers them.
+    """
+    n = 256
+    cfg = moe.make_config(T=T, d_model=n, n_experts=2, top_k=1, d_ff=n, n_shared=0, score="softmax",
+                          renormalize=True, capacity_factor=0.0, dtype="bf16")
+    one, zero = 0x38, 0x00
+    ramp = (np.arange(n)[:, None] + np.arange(n)[None, :]) % 256
+    ramp = np.where((ramp & 0x7F) == 0x7F, zero, ramp).astype(np.uint8)
+    eye = np.where(np.eye(n, dtype=bool), one, zero).astype(np.uint8)
+    ones = np.full((n, n), one, np.uint8)
+    wg, wu, wd = {"gate": (ramp, ones, eye), "up": (ones, ramp, eye), "down": (ones, eye, ramp)}[which]
+    empty = np.zeros((n, n), np.uint8)
+
+    def dev_codes(c):
+        return torch.from_numpy(np.stack([c, empty])).cuda()
+
+    scale = torch.ones(2, n, dtype=torch.float32, device="cuda")
+    xp = torch.eye(n, dtype=torch.bfloat16, device="cuda")[:T].contiguous()
+    offsets = torch.tensor([0, T, T], dtype=torch.int32, device="cuda")
+    y = torch.full((moe.moe_grouped_rows(cfg), n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(cfg)
+    moe.moe_grouped_ffn_fp8(cfg, xp, offsets, xp, dev_codes(wg), scale, dev_codes(wu), scale, dev_codes(wd),
+                            scale, y, ws)
+    assert moe.moe_get_device_error(ws) == moe.MOE_OK
+    got = to_f64(y)
+    dec = lambda c: O.e4m3_decode(c).astype(np.float64)
+    ref = O.expert_mlp(np.eye(n)[:T], dec(wg), dec(wu), dec(wd))
+    assert np.isfinite(got).all()
+    bad = np.abs(got - ref) > 2.0 ** -7 * np.abs(ref) + 1e-30
+    assert not bad.any(), f"{which}: {int(bad.sum())} outputs off, first at {np.argwhere(bad)[0]}"
