@@ -168,7 +168,7 @@ def test_fp8_refuses_float32_activations():
     assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("T", [256, 32])
+@pytest.mark.parametrize("T", [256, 32, 8])
 @pytest.mark.parametrize("which", ["gate", "up", "down"])
 def test_every_e4m3_code_widens_exactly(which, T):
     """Hand-made codes at scale 1 through moe_grouped_ffn_fp8, all tokens in expert 0.
@@ -179,7 +179,7 @@ def test_every_e4m3_code_widens_exactly(which, T):
       up    y[t,j] = silu(1) * dec(c[j,t])        (W_gate all ones, W_down the identity)
       down  y[t,j] = bf16(silu(1)) * dec(c[j,t])  (W_gate all ones, W_up the identity)
     with c[j,t] = (j + t) mod 256 sweeping every code but the two NaNs over j for each token (T=256:
-    two 128-row token tiles; T=32: one ragged tile). A wrongly widened code
+    two 128-row tiles; T=32 and T=8: one ragged tile). A wrongly widened code
     (subnormals, -0, the +-448 ends) shows as a relative error of that single output. Bound:
     one bf16 rounding of y (2^-9), the bf16 rounding of h = silu(1) in the down case (8.1e-4)
     and float32 silu; 2^-7 covers them.
