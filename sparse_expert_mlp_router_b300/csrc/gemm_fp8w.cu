@@ -18,11 +18,14 @@
 //                than the bf16 stages alone would allow
 //   warps 3-6    epilogue: per-column scales applied to the float32 accumulator
 //                (before the SwiGLU for gate/up), bf16 stores of the valid rows
-//   warps 7-14   widen the codes to bf16 into the stage's B region in the
+//   warps 7-22   widen the codes to bf16 into the stage's B region in the
 //                128-byte-swizzled K-major layout the MMA reads (the pattern a
 //                TMA SWIZZLE_128B load writes: 16-byte chunk c of row r at chunk
 //                c ^ (r mod 8)), then a proxy fence and an arrive hand the tile
-//                to the tensor cores
+//                to the tensor cores. Two groups of eight warps take alternate
+//                k-steps: a k-step's widening is a chain of waits, shared loads,
+//                conversions, stores and a fence that one group cannot shorten,
+//                so two chains run at once
 // Tiles, schedule and bounded waits are those of the bf16 single-CTA kernel.
 #include <cuda_fp8.h>
 
@@ -51,11 +54,12 @@ constexpr int kBBytes = kBRows * kBK * 2;        // 32 KB of bf16
 constexpr int kQBytes = kBRows * kBK;            // 16 KB of codes
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 4;
-constexpr int kConvWarps = 8;
-constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kConvGroups = 2;                   // converter groups, alternate k-steps
+constexpr int kConvThreads = 256;                // threads of one converter group
+constexpr int kConvWarps = kConvGroups * kConvThreads / 32;
 constexpr int kFirstEpiWarp = 3;
 constexpr int kFirstConvWarp = kFirstEpiWarp + kEpiWarps;
-constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 480
+constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 736
 constexpr int kSchedInts = 4 * (kMaxExperts + 2);
 constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kQStages * kQBytes + 512 /*barriers*/ +
                          256 * 4 /*column scales*/ + (size_t)kSchedInts * 4;
@@ -311,15 +315,15 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       if (MODE == 0) {
         __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 128;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t gv[32], uv[32];
-          ptx::tmem_ld32(t_row + c, gv);
-          ptx::tmem_ld32(t_row + 128 + c, uv);
+        for (int c = 0; c < 128; c += 16) {
+          uint32_t gv[16], uv[16];
+          ptx::tmem_ld16(t_row + c, gv);
+          ptx::tmem_ld16(t_row + 128 + c, uv);
           ptx::tmem_ld_wait();
           if (valid) {
-            uint32_t packed[16];
+            uint32_t packed[8];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+            for (int q = 0; q < 8; ++q) {
               const float g0 = __uint_as_float(gv[2 * q]) * s_scale[c + 2 * q];
               const float g1 = __uint_as_float(gv[2 * q + 1]) * s_scale[c + 2 * q + 1];
               const float u0 = __uint_as_float(uv[2 * q]) * s_scale[128 + c + 2 * q];
@@ -328,26 +332,26 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             }
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
               dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
           }
         }
       } else {
         __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 256;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_row + c, v);
+        for (int c = 0; c < 256; c += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld16(t_row + c, v);
           ptx::tmem_ld_wait();
           if (valid) {
-            uint32_t packed[16];
+            uint32_t packed[8];
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < 8; ++q)
               packed[q] = pack_bf16(__uint_as_float(v[2 * q]) * s_scale[c + 2 * q],
                                     __uint_as_float(v[2 * q + 1]) * s_scale[c + 2 * q + 1]);
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
               dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
           }
         }
@@ -357,12 +361,25 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     }
   } else {
     // ------------------------------------------------------------ code widening
-    const int ct = threadIdx.x - 32 * kFirstConvWarp;       // 0..255
-    int stage = 0, slot = 0;
+    const int cidx = threadIdx.x - 32 * kFirstConvWarp;
+    const int group = cidx / kConvThreads;                   // takes the k-steps j with j % 2 == group
+    const int ct = cidx - group * kConvThreads;              // 0..255
+    int stage = 0, slot = 0, j = 0;
     uint32_t phase = 0, qphase = 0;
     for (int L = blockIdx.x; L < total_tiles; L += gridDim.x) {
       bool ok = true;
-      for (int kb = 0; kb < k_steps; ++kb) {
+      for (int kb = 0; kb < k_steps; ++kb, ++j) {
+        if ((j % kConvGroups) != group) {                    // the other group's k-step
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++slot == kQStages) {
+            slot = 0;
+            qphase ^= 1u;
+          }
+          continue;
+        }
         if (!ptx::mbar_wait_bounded(ptx::smem_u32(&qfull[slot]), qphase, abort_flag, kWaitLimitNs) ||
             !ptx::mbar_wait_bounded(ptx::smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
