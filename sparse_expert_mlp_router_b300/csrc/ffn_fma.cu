@@ -104,8 +104,10 @@ cudaError_t launch_group_schedule(const Shape& s, const int32_t* offsets, void* 
   return cudaGetLastError();
 }
 
+// The two float32 MLP kernels; mid_event (nullable) is recorded between them.
 cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, const void* w_gate, const void* w_up,
-                           const void* w_down, const void* sched, void* h, void* y, cudaStream_t st) {
+                           const void* w_down, const void* sched, void* h, void* y, cudaStream_t st,
+                           cudaEvent_t mid_event) {
   const int64_t n_rows = s.R + (int64_t)s.S * s.T;
   const int threads = 256;
   const int64_t cap = (int64_t)num_sms() * 32;
@@ -118,6 +120,9 @@ cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, co
   ffn_gateup_fma_kernel<float><<<(unsigned)b1, threads, 0, st>>>(
       static_cast<const float*>(x_perm), static_cast<const float*>(x), static_cast<const float*>(w_gate),
       static_cast<const float*>(w_up), sc, s.G, s.E, s.d, s.F, n_rows, static_cast<float*>(h));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
   ffn_down_fma_kernel<float><<<(unsigned)b2, threads, 0, st>>>(
       static_cast<const float*>(h), static_cast<const float*>(w_down), sc, s.G, s.d, s.F, n_rows,
       static_cast<float*>(y));

@@ -134,16 +134,6 @@ moe_status_t check_ws(const Shape& s, const void* ws, size_t ws_bytes) {
 
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// A timing event: recorded as an external event node when the stream is being captured
-// into a CUDA graph, so that replays record it (a plain record would only order nodes).
-inline cudaError_t record_event(cudaEvent_t ev, cudaStream_t st) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  cudaError_t e = cudaStreamIsCapturing(st, &cs);
-  if (e != cudaSuccess) return e;
-  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
-  return cudaEventRecord(ev, st);
-}
-
 // The stage bodies, shared by the stage entry points and the whole-layer call.
 cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
                        float* gate, float* scores, int32_t* status, cudaStream_t st) {
@@ -201,8 +191,7 @@ cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_p
     if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
     return launch_gemm_down_tc(s, h, w.d, sched, y, status, st);
   }
-  if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
-  return launch_ffn_fma(s, x_perm, x, w.g, w.u, w.d, sched, h, y, st);
+  return launch_ffn_fma(s, x_perm, x, w.g, w.u, w.d, sched, h, y, st, mid_event);
 }
 
 // FP8 weights: bf16 layers whose shapes the FP8 kernels take, aligned codes and scales.
