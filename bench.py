@@ -274,6 +274,21 @@ def oracle_sample(w, n_tokens: int, one_token_batches: bool):
     return run, desc
 
 
+def max_over_ranks(ms: float, dist=None, device="cuda") -> float:
+    """The slowest rank's time (every rank passes its own; all get the maximum)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Tokens per second of the whole job: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * steps * world / (max_ms / 1e3)
+
+
 def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -394,12 +409,8 @@ def run_ours(args, w):
     status = moe.moe_get_device_error(ws)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status after timing: {moe.status_string(status)}")
-    max_ms = elapsed_ms
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-    value = w.T * K * world / (max_ms / 1e3)
+    max_ms = max_over_ranks(elapsed_ms, dist)
+    value = whole_job_rate(w.T, K, world, max_ms)
 
     # end to end: activations in pinned host memory, copies inside the timed region
     x_host = dev["x"].cpu().pin_memory()
@@ -421,12 +432,8 @@ def run_ours(args, w):
         out_host.copy_(out, non_blocking=True)
     e1.record()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = w.T * K2 * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+    e2e_value = whole_job_rate(w.T, K2, world, e2e_ms)
     if moe.moe_get_device_error(ws) != moe.MOE_OK:
         raise RuntimeError("device status after e2e timing")
 
