@@ -12,7 +12,9 @@
 //
 // One CTA per token; each thread owns 16 bytes of the row and accumulates its
 // slots in float32 in slot order, the shared row last. All loads and stores are
-// coalesced 16-byte vectors.
+// coalesced 16-byte vectors. A thread issues the loads of all its slots (kept as
+// raw 16-byte words, KM of them: k rounded up to 2, 4 or 8) before the first
+// multiply-add, so a token's k rows are in flight together.
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -24,8 +26,7 @@ struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int kN = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+  __device__ static void unpack(const uint4 u, float (&v)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -46,16 +47,15 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
   static constexpr int kN = 4;
-  __device__ static void load(const float* p, float (&v)[4]) {
-    const float4 u = *reinterpret_cast<const float4*>(p);
-    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  __device__ static void unpack(const uint4 u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y); v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
   }
   __device__ static void store(float* p, const float (&v)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
 };
 
-template <typename TE>
+template <typename TE, int KM>
 __global__ void combine_kernel(const TE* __restrict__ y, const int32_t* __restrict__ dest_row,
                                const float* __restrict__ gate, TE* __restrict__ out, int d, int k, int S, int T,
                                int64_t R, int32_t* status) {
@@ -74,21 +74,29 @@ __global__ void combine_kernel(const TE* __restrict__ y, const int32_t* __restri
   }
   __syncthreads();
   for (int c = threadIdx.x * V; c < d; c += blockDim.x * V) {
+    uint4 raw[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      const int r = j < k ? s_row[j] : -1;
+      raw[j] = r >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (size_t)r * d + c)) : make_uint4(0, 0, 0, 0);
+    }
+    uint4 shared_raw = make_uint4(0, 0, 0, 0);
+    if (S > 0) shared_raw = __ldg(reinterpret_cast<const uint4*>(y + (size_t)(R + t) * d + c));
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = s_row[j];
-      if (r < 0) continue;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      if (j >= k || s_row[j] < 0) continue;
       float v[V];
-      Vec<TE>::load(y + (size_t)r * d + c, v);
+      Vec<TE>::unpack(raw[j], v);
       const float g = s_gate[j];
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, v[i], acc[i]);
     }
-    for (int s = 0; s < S; ++s) {
+    if (S > 0) {
       float v[V];
-      Vec<TE>::load(y + (size_t)(R + (int64_t)s * T + t) * d + c, v);
+      Vec<TE>::unpack(shared_raw, v);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += v[i];
     }
@@ -120,13 +128,25 @@ cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_ro
   int threads = (s.d / V + 31) / 32 * 32;
   if (threads > 256) threads = 256;
   if (threads < 32) threads = 32;
-  if (s.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<s.T, threads, 0, st>>>(static_cast<const __nv_bfloat16*>(y), dest_row, gate,
-                                                          static_cast<__nv_bfloat16*>(out), s.d, s.k, s.S, s.T, s.R,
-                                                          status);
-  else
-    combine_kernel<float><<<s.T, threads, 0, st>>>(static_cast<const float*>(y), dest_row, gate,
-                                                  static_cast<float*>(out), s.d, s.k, s.S, s.T, s.R, status);
+  if (s.dtype == MOE_BF16) {
+    const __nv_bfloat16* yb = static_cast<const __nv_bfloat16*>(y);
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+    if (s.k <= 2)
+      combine_kernel<__nv_bfloat16, 2><<<s.T, threads, 0, st>>>(yb, dest_row, gate, ob, s.d, s.k, s.S, s.T, s.R, status);
+    else if (s.k <= 4)
+      combine_kernel<__nv_bfloat16, 4><<<s.T, threads, 0, st>>>(yb, dest_row, gate, ob, s.d, s.k, s.S, s.T, s.R, status);
+    else
+      combine_kernel<__nv_bfloat16, 8><<<s.T, threads, 0, st>>>(yb, dest_row, gate, ob, s.d, s.k, s.S, s.T, s.R, status);
+  } else {
+    const float* yf = static_cast<const float*>(y);
+    float* of = static_cast<float*>(out);
+    if (s.k <= 2)
+      combine_kernel<float, 2><<<s.T, threads, 0, st>>>(yf, dest_row, gate, of, s.d, s.k, s.S, s.T, s.R, status);
+    else if (s.k <= 4)
+      combine_kernel<float, 4><<<s.T, threads, 0, st>>>(yf, dest_row, gate, of, s.d, s.k, s.S, s.T, s.R, status);
+    else
+      combine_kernel<float, 8><<<s.T, threads, 0, st>>>(yf, dest_row, gate, of, s.d, s.k, s.S, s.T, s.R, status);
+  }
   return cudaGetLastError();
 }
 
