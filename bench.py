@@ -21,7 +21,7 @@ roofline     the dominant kernel (the gate/up grouped GEMM), timed by events rec
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload.
 --impl reference  times that oracle alone, step by step, on the host cores.
 N > 1 (torchrun): every rank runs its own replica of the layer (the layer has no
-exchange step; see DESIGN.md), value = all ranks' tokens / max time.
+exchange step), value = all ranks' tokens / max time.
 """
 from __future__ import annotations
 
@@ -437,14 +437,20 @@ def run_ours(args, w):
     if moe.moe_get_device_error(ws) != moe.MOE_OK:
         raise RuntimeError("device status after e2e timing")
 
-    # roofline of the dominant kernel: the gate/up grouped GEMM (stage 2 -> 3)
+    # roofline of the dominant kernel: the gate/up grouped GEMM (stage 2 -> 3). A tensor-bound
+    # kernel timed inside a long run of back-to-back layers (>= 1 s, where the GPU settles at
+    # its power limit) is compared with the sustained bf16 rate, else with the burst rate; the
+    # fraction of the burst rate is reported as well.
     peaks, peak_src = load_peaks()
     gemm_ms = float(stage[:, 2].mean())
     t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * 1e12)
     t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    long_run = max_ms >= 1000.0
     if t_tensor >= t_bytes:
         achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac_of_burst": achieved / peaks["bf16_tflops"]}
     else:
         achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
@@ -452,7 +458,9 @@ def run_ours(args, w):
     roof["traffic"] = measured_traffic(w.name, args.weights)
     roof["kernel"] = ("grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
                       "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
-    roof["peak_source"] = f"{peak_src} burst" if roof["bound"] == "tensor" else f"{peak_src} copy bandwidth"
+    roof["peak_source"] = (f"{peak_src} copy bandwidth" if roof["bound"] == "hbm" else
+                           f"{peak_src} sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else
+                           f"{peak_src} burst")
     roof["ms_per_launch"] = gemm_ms
 
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
