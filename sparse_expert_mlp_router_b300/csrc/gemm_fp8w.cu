@@ -26,7 +26,15 @@
 //                k-steps: a k-step's widening is a chain of waits, shared loads,
 //                conversions, stores and a fence that one group cannot shorten,
 //                so two chains run at once
-// Tiles, schedule and bounded waits are those of the bf16 single-CTA kernel.
+// Tiles and bounded waits are those of the bf16 single-CTA kernel.
+//
+// Decode-shaped layers (at most 8 pairs per expert on average, reduction <= 2048) run a
+// resident-token variant: tiles of 8 token rows whose A operand for the whole reduction
+// (K/64 boxes of 8 rows x 64 bf16, 1 KB each) is loaded once per tile into its own buffer,
+// and the M=128 MMA reads it through a descriptor whose 8-row group stride is 0, so rows
+// 8..127 repeat rows 0..7 and are masked in the epilogue. The stages then hold only the
+// widened weights, the per-k-step token tile (which otherwise waits behind the SM's code
+// reads) disappears, and the freed memory deepens the code ring.
 #include <cuda_fp8.h>
 
 #include "gemm_common.cuh"
@@ -46,13 +54,21 @@ using gemm::silu_f;
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 3;                       // A + widened B per stage
-constexpr int kQStages = 4;                      // weight codes per slot
+constexpr int kStages = 3;                       // (A +) widened B per stage
+constexpr int kMaxQSlots = 8;                    // weight-code slots (4 with per-k-step A tiles)
+constexpr int kResRows = 8;                      // token rows of a resident-token tile
 constexpr int kABytes = kBM * kBK * 2;           // 16 KB
 constexpr int kBRows = 256;                      // gate/up: 128 W_gate + 128 W_up rows; down: 256 W_down rows
 constexpr int kBBytes = kBRows * kBK * 2;        // 32 KB of bf16
 constexpr int kQBytes = kBRows * kBK;            // 16 KB of codes
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kResBoxBytes = kResRows * kBK * 2; // 1 KB: 8 token rows of one k-step
+
+template <bool RES>
+struct FCfg {
+  static constexpr int kStageBytes = RES ? kBBytes : kABytes + kBBytes;
+  static constexpr int kBOff = RES ? 0 : kABytes;   // B within a stage
+  static constexpr int kRows = RES ? kResRows : kBM;  // token rows of a tile
+};
 constexpr int kEpiWarps = 4;
 constexpr int kConvGroups = 2;                   // converter groups, alternate k-steps
 constexpr int kConvThreads = 256;                // threads of one converter group
@@ -61,8 +77,9 @@ constexpr int kFirstEpiWarp = 3;
 constexpr int kFirstConvWarp = kFirstEpiWarp + kEpiWarps;
 constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);   // 736
 constexpr int kSchedInts = 4 * (kMaxExperts + 2);
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kQStages * kQBytes + 512 /*barriers*/ +
-                         256 * 4 /*column scales*/ + (size_t)kSchedInts * 4;
+constexpr size_t kSmemFixed = 1024 /*alignment*/ + 512 /*barriers*/ + 256 * 4 /*column scales*/ +
+                              (size_t)kSchedInts * 4;
+constexpr size_t kSmemMax = 232448;
 
 struct Fp8Args {
   int K;                 // reduction length
@@ -71,6 +88,8 @@ struct Fp8Args {
   int shared_from;       // groups >= shared_from read A from the second A map (gate/up only)
   int b_rows;            // weight rows per group (F for gate/up, d for down)
   const int32_t* sched;  // device group schedule
+  int qslots;            // weight-code slots (<= kMaxQSlots)
+  int res_bytes;         // resident-token buffer (K/64 KB) when tiles are 8 rows, else 0
   const float* scale;    // gate/up: W_gate row scales [G, F]; down: W_down row scales [G, d]
   const float* scale2;   // gate/up: W_up row scales [G, F]
   __nv_bfloat16* out;
@@ -92,7 +111,7 @@ __device__ __forceinline__ uint32_t widen2(uint32_t pair) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int MODE>
+template <int MODE, bool RES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQ2,
@@ -100,18 +119,23 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);   // 1024-byte aligned
+  using C = FCfg<RES>;
+  const int kQStages = args.qslots;
   uint8_t* stage_base = smem;
-  uint8_t* code_base = smem + (size_t)kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(code_base + (size_t)kQStages * kQBytes);
-  uint64_t* full = bars;                       // [kStages] A landed
+  uint8_t* code_base = smem + (size_t)kStages * C::kStageBytes;
+  uint8_t* a_res = code_base + (size_t)kQStages * kQBytes;            // resident-token tile (RES)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(a_res + args.res_bytes);
+  uint64_t* full = bars;                       // [kStages] A landed (per-k-step A tiles)
   uint64_t* conv = full + kStages;             // [kStages] B widened
   uint64_t* empty = conv + kStages;            // [kStages] stage read by the MMAs
-  uint64_t* qfull = empty + kStages;           // [kQStages] codes landed
-  uint64_t* qempty = qfull + kQStages;         // [kQStages] codes read by the converters
-  uint64_t* tfull = qempty + kQStages;         // [2]
+  uint64_t* qfull = empty + kStages;           // [qslots] codes landed
+  uint64_t* qempty = qfull + kMaxQSlots;       // [qslots] codes read by the converters
+  uint64_t* tfull = qempty + kMaxQSlots;       // [2]
   uint64_t* tempty = tfull + 2;                // [2]
   uint64_t* drain = tempty + 2;                // [1]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* afull = drain + 1;                 // [1] resident-token tile landed (RES)
+  uint64_t* aempty = afull + 1;                // [1] resident-token tile read by the MMAs (RES)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(aempty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_stop = reinterpret_cast<volatile int*>(tmem_holder + 2);   // epilogue's snapshot
   float* s_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);   // [256]
@@ -123,8 +147,29 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  for (int i = threadIdx.x; i < 4 * args.G + 1; i += kThreads) s_tile_start[i] = args.sched[i];
+  // The schedule's rows, and a prefix of this kernel's m-tiles (C::kRows token rows each).
+  for (int i = args.G + 1 + threadIdx.x; i < 4 * args.G + 1; i += kThreads) s_tile_start[i] = args.sched[i];
+  if (warp == 0) {
+    const int32_t* n_rows = args.sched + (args.G + 1) + 2 * args.G;
+    int carry = 0;
+    for (int base = 0; base < args.G; base += 32) {
+      const int g = base + lane;
+      const int r = g < args.G ? n_rows[g] : 0;
+      const int tiles = (r + C::kRows - 1) / C::kRows;
+      int incl = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < args.G) s_tile_start[g] = carry + incl - tiles;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_tile_start[args.G] = carry;
+  }
   if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(afull), 1);
+    ptx::mbar_init(ptx::smem_u32(aempty), 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&conv[s]), kConvThreads);
@@ -164,7 +209,32 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
   if (warp == 0) {
     // ------------------------------------------------------------ A producer
-    if (lane == 0) {
+    if (lane == 0 && RES) {
+      // one resident-token tile per tile: K/64 boxes of 8 rows into the resident buffer
+      int it = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < total_tiles; L += gridDim.x, ++it) {
+        int g, m, n;
+        decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
+        const bool use_a2 = (MODE == 0) && (g >= args.shared_from);
+        const int a_row = ((MODE == 0) ? s_a_row[g] : s_out_row[g]) + m * kResRows;
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(aempty), (uint32_t)(it & 1) ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = ptx::smem_u32(afull);
+        ptx::mbar_arrive_expect_tx(fb, (uint32_t)(k_steps * kResBoxBytes));
+        for (int kb = 0; kb < k_steps; ++kb)
+          ptx::tma_load_2d(ptx::smem_u32(a_res + (size_t)kb * kResBoxBytes),
+                           use_a2 ? (const void*)&tmA2 : (const void*)&tmA, kb * kBK, a_row, fb);
+      }
+      if (!ok) {
+        set_status(args.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // the last resident tile issued lands before the shared memory is left
+      if (it > 0) ptx::mbar_wait_bounded(ptx::smem_u32(afull), (uint32_t)((it - 1) & 1), nullptr, kDrainLimitNs);
+    } else if (lane == 0) {
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -180,7 +250,7 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           }
           const uint32_t fb = ptx::smem_u32(&full[stage]);
           ptx::mbar_arrive_expect_tx(fb, kABytes);
-          ptx::tma_load_2d(ptx::smem_u32(stage_base + (size_t)stage * kStageBytes),
+          ptx::tma_load_2d(ptx::smem_u32(stage_base + (size_t)stage * C::kStageBytes),
                            use_a2 ? (const void*)&tmA2 : (const void*)&tmA, kb * kBK, a_row, fb);
           if (issued < kStages) ++issued;
           if (++stage == kStages) {
@@ -236,7 +306,8 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, 256);
+      // resident-token tiles hold at most 8 rows: an M=64 MMA (rows 0-15 in TMEM lanes 0-15)
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(RES ? 64 : kBM, 256);
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -247,18 +318,23 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           ok = false;
           break;
         }
+        if (RES && !ptx::mbar_wait_bounded(ptx::smem_u32(afull), (uint32_t)(it & 1), abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
         for (int kb = 0; kb < k_steps; ++kb) {
-          if (!ptx::mbar_wait_bounded(ptx::smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
+          if ((!RES && !ptx::mbar_wait_bounded(ptx::smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) ||
               !ptx::mbar_wait_bounded(ptx::smem_u32(&conv[stage]), phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(stage_base + (size_t)stage * kStageBytes);
-          const uint64_t a_desc = ptx::sw128_kmajor_desc(sa);
-          const uint64_t b_desc = ptx::sw128_kmajor_desc(sa + kABytes);
+          const uint32_t sa = ptx::smem_u32(stage_base + (size_t)stage * C::kStageBytes);
+          const uint64_t a_desc = RES ? ptx::sw128_kmajor_desc_rows8(ptx::smem_u32(a_res + (size_t)kb * kResBoxBytes))
+                                      : ptx::sw128_kmajor_desc(sa);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(sa + C::kBOff);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             ptx::mma_bf16(d_tmem, a_desc + (uint64_t)(2 * kk), b_desc + (uint64_t)(2 * kk), idesc,
@@ -270,6 +346,7 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           }
         }
         if (!ok) break;
+        if (RES) ptx::mma_commit(ptx::smem_u32(aempty));     // the tile's MMAs are done with its tokens
         ptx::mma_commit(ptx::smem_u32(&tfull[acc]));
       }
       if (!ok) {
@@ -309,8 +386,8 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       epi_bar();
       if (*s_stop != 0) break;
       ptx::tc_fence_after();
-      const bool valid = (m * kBM + r_local) < s_rows[g];
-      const int64_t out_row = (int64_t)s_out_row[g] + m * kBM + r_local;
+      const bool valid = r_local < C::kRows && (m * C::kRows + r_local) < s_rows[g];
+      const int64_t out_row = (int64_t)s_out_row[g] + m * C::kRows + r_local;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256);
       if (MODE == 0) {
         __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 128;
@@ -386,7 +463,7 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           break;
         }
         const uint8_t* codes = code_base + (size_t)slot * kQBytes;
-        uint8_t* bdst = stage_base + (size_t)stage * kStageBytes + kABytes;
+        uint8_t* bdst = stage_base + (size_t)stage * C::kStageBytes + C::kBOff;
 #pragma unroll
         for (int u = 0; u < (kBRows * 4) / kConvThreads; ++u) {
           const int t = ct + u * kConvThreads;
@@ -475,21 +552,38 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ w, in
   }
 }
 
-template <int MODE>
+// Resident-token tiles where the average expert holds at most 8 pairs (decode) and the tile's
+// tokens for the whole reduction (K/64 KB) leave at least four code slots.
+bool use_resident(const Shape& s, int K) {
+  return (int64_t)s.T * s.k <= (int64_t)kResRows * s.E && K <= 2048;
+}
+
+// Upper bound on a launch's m-tiles of `rows` token rows: the routed rows spread over E groups
+// (each may add one partial tile) plus the shared groups' rows.
+int64_t max_m_tiles(const Shape& s, int rows) {
+  return (s.R + rows - 1) / rows + s.E + (int64_t)s.S * ((s.T + rows - 1) / rows);
+}
+
+template <int MODE, bool RES>
 cudaError_t launch_fp8w(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& q, const CUtensorMap& q2,
-                        const Fp8Args& args, int64_t max_tiles, cudaStream_t st) {
-  auto kern = grouped_gemm_fp8w_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+                        Fp8Args args, const Shape& s, cudaStream_t st) {
+  using C = FCfg<RES>;
+  args.res_bytes = RES ? (args.K / kBK) * kResBoxBytes : 0;
+  const size_t base = kSmemFixed + (size_t)kStages * C::kStageBytes + (size_t)args.res_bytes;
+  int q_slots = RES ? (int)((kSmemMax - base) / kQBytes) : 4;
+  if (q_slots > kMaxQSlots) q_slots = kMaxQSlots;
+  if (q_slots < 2) return cudaErrorInvalidValue;
+  args.qslots = q_slots;
+  const size_t smem = base + (size_t)q_slots * kQBytes;
+  auto kern = grouped_gemm_fp8w_kernel<MODE, RES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  const int64_t max_tiles = max_m_tiles(s, C::kRows) * args.n_tiles;
   int64_t grid = num_sms();
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads, kSmem, st>>>(a, a2, q, q2, args);
+  kern<<<(unsigned)grid, kThreads, smem, st>>>(a, a2, q, q2, args);
   return cudaGetLastError();
-}
-
-int64_t max_m_tiles(const Shape& s) {
-  return (s.R + kBM - 1) / kBM + s.E + (int64_t)s.S * ((s.T + kBM - 1) / kBM);
 }
 
 }  // namespace
@@ -512,8 +606,10 @@ cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const vo
                                     void* h, int32_t* status, cudaStream_t st) {
   CUtensorMap a, a2, q, q2;
   const uint64_t R = (uint64_t)(s.R > 0 ? s.R : 1);
-  if (!make_tmap_bf16(&a, x_perm, s.d, R, kBM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&a2, s.S > 0 ? x : x_perm, s.d, s.S > 0 ? (uint64_t)s.T : R, kBM)) return cudaErrorInvalidValue;
+  const bool res = use_resident(s, s.d);
+  const uint32_t box = res ? kResRows : kBM;
+  if (!make_tmap_bf16(&a, x_perm, s.d, R, box)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&a2, s.S > 0 ? x : x_perm, s.d, s.S > 0 ? (uint64_t)s.T : R, box)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&q, wg_q, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&q2, wu_q, s.d, (uint64_t)s.G * s.F, 128)) return cudaErrorInvalidValue;
   Fp8Args args{};
@@ -528,14 +624,15 @@ cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const vo
   args.out = static_cast<__nv_bfloat16*>(h);
   args.ldo = s.F;
   args.status = status;
-  return launch_fp8w<0>(a, a2, q, q2, args, max_m_tiles(s) * args.n_tiles, st);
+  return res ? launch_fp8w<0, true>(a, a2, q, q2, args, s, st) : launch_fp8w<0, false>(a, a2, q, q2, args, s, st);
 }
 
 cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* wd_q, const float* wd_s,
                                   const void* sched, void* y, int32_t* status, cudaStream_t st) {
   CUtensorMap a, q;
   const uint64_t rows = (uint64_t)s.R + (uint64_t)s.S * s.T;
-  if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
+  const bool res = use_resident(s, s.F);
+  if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, res ? kResRows : kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&q, wd_q, s.F, (uint64_t)s.G * s.d, 128)) return cudaErrorInvalidValue;
   Fp8Args args{};
   args.K = s.F;
@@ -549,7 +646,7 @@ cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* 
   args.out = static_cast<__nv_bfloat16*>(y);
   args.ldo = s.d;
   args.status = status;
-  return launch_fp8w<1>(a, a, q, q, args, max_m_tiles(s) * args.n_tiles, st);
+  return res ? launch_fp8w<1, true>(a, a, q, q, args, s, st) : launch_fp8w<1, false>(a, a, q, q, args, s, st);
 }
 
 }  // namespace moe

@@ -156,6 +156,12 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// The same operand with an 8-row group stride of 0: an M=128 read of the 1 KB swizzle atom
+// at smem_addr (8 rows x 64 bf16), in which rows 8..127 repeat rows 0..7.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc_rows8(uint32_t smem_addr) {
+  return sw128_kmajor_desc(smem_addr) & ~((uint64_t)0x3FFF << 32);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, float32 D,
 // both operands K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
