@@ -172,12 +172,12 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     ptx::mbar_init(ptx::smem_u32(aempty), 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(ptx::smem_u32(&full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&conv[s]), kConvThreads);
+      ptx::mbar_init(ptx::smem_u32(&conv[s]), kConvThreads / 32);      // one arrive per converter warp
       ptx::mbar_init(ptx::smem_u32(&empty[s]), 1);
     }
     for (int q = 0; q < kQStages; ++q) {
       ptx::mbar_init(ptx::smem_u32(&qfull[q]), 1);
-      ptx::mbar_init(ptx::smem_u32(&qempty[q]), kConvThreads);
+      ptx::mbar_init(ptx::smem_u32(&qempty[q]), kConvThreads / 32);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_u32(&tfull[a]), 1);
@@ -475,9 +475,15 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
           *reinterpret_cast<uint4*>(rowp + (((2 * j) ^ (r & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(rowp + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
         }
-        fence_proxy_async_smem();                            // widened tile visible to the MMA
-        ptx::mbar_arrive(ptx::smem_u32(&conv[stage]));
-        ptx::mbar_arrive(ptx::smem_u32(&qempty[slot]));
+        // Each thread's widened stores are made visible to the async proxy, then one lane per
+        // warp hands the warp's part to the MMA and frees its codes (8 arrives, not 256 that
+        // would serialise on the barrier).
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(ptx::smem_u32(&conv[stage]));
+          ptx::mbar_arrive(ptx::smem_u32(&qempty[slot]));
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
