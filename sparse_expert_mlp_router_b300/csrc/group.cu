@@ -154,6 +154,67 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ idx, int T, int
   }
 }
 
+// The three steps above in one CTA when the batch is a single chunk (T <= 128, decode): the
+// chunk's masks once, per-expert counts, capacity clamp and scan, the group schedule, then
+// the scatter, with the same ranks as the three-kernel path (chunk base 0).
+__global__ void __launch_bounds__(kScanThreads)
+group_single_chunk_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int cap,
+                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                          int32_t* __restrict__ dest_row, int32_t* __restrict__ src_token,
+                          int32_t* __restrict__ sched, int S, int64_t R, int32_t* status) {
+  __shared__ uint32_t mask[kMaxExperts * kWords];
+  __shared__ bool dup[kChunk * kMaxTopK];
+  __shared__ int32_t warp_tot[kScanThreads / 32];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  build_masks(mask, idx, 0, T, k, E, status, dup);
+  const int e = threadIdx.x;
+  int n = 0;
+  if (e < E) {
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) n += __popc(mask[e * kWords + w]);
+    counts[e] = n;
+  }
+  const int kv = (e < E) ? min(n, cap) : 0;
+  const int lane = e & 31, warp = e >> 5;
+  int incl = kv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += warp_tot[w];
+  if (e < E) {
+    offsets[e] = base + incl - kv;
+    s_off[e] = base + incl - kv;
+  }
+  if (e == kScanThreads - 1) {
+    offsets[E] = base + incl;
+    s_off[E] = base + incl;
+  }
+  __syncthreads();
+  if (sched != nullptr && warp == 0) build_schedule_warp(s_off, false, E, S, T, R, sched);
+  for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
+    const int t = p / k;
+    const int ex = idx[p];
+    int row = -1;
+    if (!dup[p]) {
+      const uint32_t* m = mask + ex * kWords;
+      int r = 0;
+      for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
+      r += __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+      const int lo = s_off[ex], hi = s_off[ex + 1];
+      if (r < hi - lo) {
+        row = lo + r;
+        src_token[row] = t;
+      }
+    }
+    dest_row[p] = row;
+  }
+}
+
 // x_perm[r] = x[src_token[r]] for r < offsets[E]; one warp per row, 16-byte vectors.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src_token,
                                    const int32_t* __restrict__ offsets, int E, int vec_per_row, int64_t R,
@@ -197,6 +258,15 @@ cudaError_t launch_group_scatter(const Shape& s, const int32_t* idx, const int32
                                  const int32_t* offsets, int32_t* dest_row, int32_t* src_token,
                                  cudaStream_t st) {
   group_scatter_kernel<<<s.nchunks, 256, 0, st>>>(idx, s.T, s.k, s.E, chunk_base, offsets, dest_row, src_token);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                      int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                      cudaStream_t st) {
+  if (s.nchunks != 1) return cudaErrorInvalidValue;
+  group_single_chunk_kernel<<<1, kScanThreads, 0, st>>>(idx, s.T, s.k, s.E, s.cap, counts, offsets, dest_row,
+                                                        src_token, static_cast<int32_t*>(sched), s.S, s.R, status);
   return cudaGetLastError();
 }
 

@@ -92,6 +92,10 @@ cudaError_t launch_group_scan(const Shape& s, int32_t* chunk_counts, int32_t* co
 cudaError_t launch_group_scatter(const Shape& s, const int32_t* idx, const int32_t* chunk_base,
                                  const int32_t* offsets, int32_t* dest_row, int32_t* src_token,
                                  cudaStream_t st);
+// hist + scan (+ schedule) + scatter in one CTA; only for a single chunk (T <= kChunk).
+cudaError_t launch_group_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                      int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                      cudaStream_t st);
 cudaError_t launch_gather_rows(const Shape& s, const void* x, const int32_t* src_token,
                                const int32_t* offsets, void* x_perm, cudaStream_t st);
 

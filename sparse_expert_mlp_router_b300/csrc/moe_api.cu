@@ -149,6 +149,12 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
   cudaError_t e;
+  if (s.nchunks == 1) {       // one chunk of tokens (decode): the three grouping steps in one CTA
+    if ((e = launch_group_single_chunk(s, idx, counts, offsets, dest_row, src_token,
+                                       with_schedule ? at<void>(ws, L.sched) : nullptr, status, st)) != cudaSuccess)
+      return e;
+    return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
+  }
   if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
   if ((e = launch_group_scan(s, cc, counts, offsets, with_schedule ? at<void>(ws, L.sched) : nullptr, st)) !=
       cudaSuccess)
@@ -207,9 +213,9 @@ moe_status_t check_fp8_weights(const Shape& s, const uint8_t* wg_q, const float*
 
 // Kernel launches one moe_layer_forward enqueues.
 int layer_launches(const Shape& s) {
-  // hist, scan (+ group schedule), scatter, gather
-  const int router = 1, grouping = 4, mlp = 2, combine = 1;
-  (void)s;
+  // hist, scan (+ group schedule), scatter, gather; one CTA for the first three when the batch
+  // is a single chunk of tokens
+  const int router = 1, grouping = s.nchunks == 1 ? 2 : 4, mlp = 2, combine = 1;
   return router + grouping + mlp + combine;
 }
 
