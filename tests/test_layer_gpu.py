@@ -89,6 +89,36 @@ def test_layer_repeatable():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("name,edit", [
+    ("mini_deepseek", dict(T=64, n_experts=256, top_k=8)),        # the most experts
+    ("mini_deepseek", dict(T=64, n_experts=149, top_k=6)),        # one past the SM count
+    ("mini_qwen3", dict(T=33, n_experts=148, top_k=4)),           # tokens not a multiple of 8
+    ("mini_decode", dict(T=1, n_experts=5, top_k=2)),
+    ("tiny_f32", dict(T=40, d_model=72, score="sigmoid")),
+])
+def test_layer_small_batches_repeat_on_one_workspace(name, edit):
+    # Decode-sized batches with expert counts around and above the SM count, called three times
+    # on one workspace: every call routes and computes identically, and matches the oracle.
+    w = synth.WORKLOADS[name].with_(**edit)
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    ws = moe.alloc_workspace(cfg)
+    outs, idxs = [], []
+    for _ in range(3):
+        out = torch.full((w.T, w.d_model), float("nan"), dtype=dev["x"].dtype, device="cuda")
+        idx = torch.full((w.T, w.top_k), -1, dtype=torch.int32, device="cuda")
+        moe.moe_layer_forward(cfg, dev["x"], dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"],
+                              dev["w_down"], out, ws, topk_idx_out=idx)
+        assert moe.moe_get_device_error(ws) == moe.MOE_OK
+        outs.append(out)
+        idxs.append(idx.cpu().numpy())
+    assert all((i == idxs[0]).all() for i in idxs[1:])
+    assert all(torch.equal(o, outs[0]) for o in outs[1:])
+    res, _ = _oracle_on_gpu_routing(w, inp.f64["x"], inp.f64["w_router"], inp.bias, inp.expert, idxs[0])
+    assert_close(to_f64(outs[0]), res.out, out_tolerance(w), f"{name} {edit}")
+
+
 # ------------------------------------------------------------- full sizes
 
 def _sample_tokens(w, idx, dest_row, n=12):
