@@ -15,7 +15,9 @@ value        tokens/s with inputs resident in HBM, K steps timed with CUDA event
              same kernels as an eager one.
 e2e          the same metric through the same C-ABI call with the activations in
              pinned host memory: each step copies x host->device, runs the layer and
-             copies out device->host.
+             copies out device->host. Steps with at least 1 MB of activations run their
+             copies on their own streams, overlapping the neighbouring steps' layers;
+             smaller steps run serially on one stream. Both loops are reported.
 roofline     the dominant kernel (the gate/up grouped GEMM), timed by events recorded
              around it inside the timed region on the launching stream.
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload.
@@ -41,6 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s on 1 B300"
 UNIT = "tokens/s"
+OVERLAP_MIN_BYTES = 1 << 20          # end-to-end loop: overlap the copies from this size
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -412,28 +415,69 @@ def run_ours(args, w):
     max_ms = max_over_ranks(elapsed_ms, dist)
     value = whole_job_rate(w.T, K, world, max_ms)
 
-    # end to end: activations in pinned host memory, copies inside the timed region
+    # end to end: activations in pinned host memory, copies inside the timed region. Two loops:
+    # serial (one stream: copy x in, run the layer, copy the output out), and overlapped (the
+    # copies on their own streams, two device buffers of each, so that step i's copies overlap
+    # the layers of steps i-1 and i+1). Cross-stream waits cost a few microseconds a step, more
+    # than copies of a few hundred KB take, so the reported loop is the overlapped one when a
+    # step's activations reach OVERLAP_MIN_BYTES and the serial one below; both are reported.
     x_host = dev["x"].cpu().pin_memory()
-    out_host = torch.empty(out.shape, dtype=dt).pin_memory()
-    x_dev = torch.empty_like(dev["x"])
-    args_e2e = (cfg, x_dev, dev["w_router"], dev["bias"], *wargs, out, ws)
+    out_hosts = [torch.empty(out.shape, dtype=dt).pin_memory() for _ in range(2)]
+    x_devs = [torch.empty_like(dev["x"]) for _ in range(2)]
+    out_devs = [out, torch.empty_like(out)]
+    main = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # x_devs[b] holds this step's input
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # the layer on buffer pair b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # out_devs[b] copied to the host
+
+    def e2e_step(i):
+        b = i % 2
+        h2d.wait_event(ev_done[b])                       # the layer that read x_devs[b] is done
+        with torch.cuda.stream(h2d):
+            x_devs[b].copy_(x_host, non_blocking=True)
+        ev_in[b].record(h2d)
+        main.wait_event(ev_in[b])
+        main.wait_event(ev_out[b])                       # out_devs[b] is free again
+        forward(cfg, x_devs[b], dev["w_router"], dev["bias"], *wargs, out_devs[b], ws)
+        ev_done[b].record(main)
+        d2h.wait_event(ev_done[b])
+        with torch.cuda.stream(d2h):
+            out_hosts[b].copy_(out_devs[b], non_blocking=True)
+        ev_out[b].record(d2h)
+
+    def e2e_serial_step():
+        x_devs[0].copy_(x_host, non_blocking=True)
+        forward(cfg, x_devs[0], dev["w_router"], dev["bias"], *wargs, out_devs[0], ws)
+        out_hosts[0].copy_(out_devs[0], non_blocking=True)
+
     K2 = max(args.e2e_steps, 1)
     for _ in range(3):
-        x_dev.copy_(x_host, non_blocking=True)
-        forward(*args_e2e)
-        out_host.copy_(out, non_blocking=True)
+        e2e_serial_step()
+    torch.cuda.synchronize()
+    for i in range(4):
+        e2e_step(i)
+    torch.cuda.synchronize()                             # the two loops share buffer 0
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(K2):
-        x_dev.copy_(x_host, non_blocking=True)
-        forward(*args_e2e)
-        out_host.copy_(out, non_blocking=True)
+    for i in range(K2):
+        e2e_serial_step()
     e1.record()
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist)
-    e2e_value = whole_job_rate(w.T, K2, world, e2e_ms)
+    serial_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+    e0.record()
+    h2d.wait_stream(main)
+    d2h.wait_stream(main)
+    for i in range(K2):
+        e2e_step(i)
+    main.wait_stream(d2h)                                # the last output has reached the host
+    e1.record()
+    barrier()
+    overlap_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+    overlapped = x_host.numel() * x_host.element_size() >= OVERLAP_MIN_BYTES
+    e2e_value = whole_job_rate(w.T, K2, world, overlap_ms if overlapped else serial_ms)
     if moe.moe_get_device_error(ws) != moe.MOE_OK:
         raise RuntimeError("device status after e2e timing")
 
@@ -489,7 +533,12 @@ def run_ours(args, w):
                    "launch": "eager" if args.eager else "cuda_graph",
                    "weights": "fp8 e4m3, per-row float32 scales" if fp8 else w.dtype},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": K2,
+                "copies": ("own streams, overlapping the neighbouring steps' layers (double-buffered)"
+                           if overlapped else "serial, on the layer's stream (activations under %d bytes)"
+                           % OVERLAP_MIN_BYTES),
+                "serial_value": whole_job_rate(w.T, K2, world, serial_ms),
+                "overlapped_value": whole_job_rate(w.T, K2, world, overlap_ms)},
         "gpu_launches": K * moe.moe_layer_launch_count(cfg),
         "roofline": roof,
         "cpu_baseline": cpu,
