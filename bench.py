@@ -12,14 +12,16 @@ value        tokens/s with inputs resident in HBM, K steps timed with CUDA event
              (2.8 GB) exceed the 126 MB L2, so every step streams them from HBM.
              The K moe_layer_forward calls are captured into one CUDA graph and
              replayed (--eager: K separate calls); each captured call enqueues the
-             same kernels as an eager one.
+             same kernels as an eager one. Stage times (and the roofline's kernel
+             time) come from a second replay of the same K calls with CUDA events
+             at the stage boundaries (--eager: from the timed calls themselves).
 e2e          the same metric through the same C-ABI call with the activations in
              pinned host memory: each step copies x host->device, runs the layer and
              copies out device->host. Steps with at least 1 MB of activations run their
              copies on their own streams, overlapping the neighbouring steps' layers;
              smaller steps run serially on one stream. Both loops are reported.
 roofline     the dominant kernel (the gate/up grouped GEMM), timed by events recorded
-             around it inside the timed region on the launching stream.
+             around it on the launching stream, in the staged replay of the K layers.
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload.
 --impl reference  times that oracle alone, step by step, on the host cores.
 N > 1 (torchrun): every rank runs its own replica of the layer (the layer has no
@@ -44,6 +46,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s on 1 B300"
 UNIT = "tokens/s"
 OVERLAP_MIN_BYTES = 1 << 20          # end-to-end loop: overlap the copies from this size
+E2E_WARM_S = 0.3                     # end-to-end loops: warm-up wall time
+E2E_MIN_S = 0.3                      # end-to-end loops: least timed device time
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -56,7 +60,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mixtral_8x7b")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="end-to-end steps per loop (default: at least 100 and 0.3 s of layers)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
@@ -380,13 +385,22 @@ def run_ours(args, w):
     for i in range(W):
         forward_timed(*args_fwd, evs[i % K])
     barrier()
-    graph = None
+    # Graph mode: the timed region replays K plain moe_layer_forward calls; the stage times come
+    # from a second replay of the same K calls with CUDA events recorded at the stage boundaries
+    # (six event records a layer cost the decode-shaped layer about 8 %). Eager mode (--eager,
+    # for profilers): K calls with the stage events, timed as they run.
+    graph = graph_staged = None
     if not args.eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(K):
+                forward(*args_fwd)
+        graph_staged = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_staged):
+            for i in range(K):
                 forward_timed(*args_fwd, evs[i])
-        graph.replay()         # one untimed replay
+        graph.replay()         # one untimed replay of each
+        graph_staged.replay()
         barrier()
     props = torch.cuda.get_device_properties(local)
     try:
@@ -406,6 +420,9 @@ def run_ours(args, w):
             forward_timed(*args_fwd, evs[i])
     t_end.record()
     barrier()
+    if graph_staged is not None:
+        graph_staged.replay()
+        barrier()
     clocks = sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])   # [K, 5] ms
@@ -451,22 +468,32 @@ def run_ours(args, w):
         forward(cfg, x_devs[0], dev["w_router"], dev["bias"], *wargs, out_devs[0], ws)
         out_hosts[0].copy_(out_devs[0], non_blocking=True)
 
-    K2 = max(args.e2e_steps, 1)
-    for _ in range(3):
-        e2e_serial_step()
-    torch.cuda.synchronize()
-    for i in range(4):
-        e2e_step(i)
-    torch.cuda.synchronize()                             # the two loops share buffer 0
-    barrier()
+    # By default each loop is warmed up for E2E_WARM_S of wall time (the host's clock settles: a
+    # cold host doubled the per-step cost of the smallest layers) and timed over at least
+    # E2E_MIN_S of steps; --e2e-steps N times exactly N steps after a few warm-up steps.
+    auto = args.e2e_steps is None
+    K2 = max(100, math.ceil(E2E_MIN_S / (max_ms / K / 1e3))) if auto else max(args.e2e_steps, 1)
+
+    def warm(fn, n_min):
+        t_end = time.perf_counter() + (E2E_WARM_S if auto else 0.0)
+        i = 0
+        while i < n_min or time.perf_counter() < t_end:
+            fn(i)
+            i += 1
+        torch.cuda.synchronize()
+
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    warm(lambda i: e2e_serial_step(), 3)
+    barrier()
     e0.record()
     for i in range(K2):
         e2e_serial_step()
     e1.record()
     barrier()
     serial_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+    warm(e2e_step, 4)                                    # the two loops share buffer 0: synchronised
+    barrier()
     e0.record()
     h2d.wait_stream(main)
     d2h.wait_stream(main)
