@@ -141,9 +141,17 @@ class ClockSampler:
             self.proc.kill()
         self.tmp.flush()
         self.tmp.seek(0)
+        text = self.tmp.read()
+        os.unlink(self.tmp.name)
+        return self.parse(text)
+
+    @staticmethod
+    def parse(text: str) -> dict:
+        """Median SM clock, highest max clock and power, and every throttle reason seen active,
+        from nvidia-smi CSV lines in FIELDS order (malformed lines are skipped)."""
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.tmp.read().splitlines():
+        for line in text.splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -156,7 +164,6 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
-        os.unlink(self.tmp.name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
