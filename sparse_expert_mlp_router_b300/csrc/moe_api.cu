@@ -4,6 +4,8 @@
 #include <cmath>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -120,6 +122,16 @@ WsLayout make_layout(const Shape& s) {
 using namespace moe;
 
 namespace {
+
+// NVTX range over a scope (host-side; a profiler shows the kernels each stage enqueues under
+// its name, e.g. ncu --nvtx --nvtx-include "moe_layer/experts/"). Without a tool attached the
+// calls return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -250,15 +262,28 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   void* y = at<void>(ws, L.y);
 
   auto mark = [&](int i) { return ev[i] == nullptr || record_event(ev[i], st) == cudaSuccess; };
+  const NvtxRange layer_range("moe_layer");
   if (!mark(0)) return MOE_ERR_CUDA;
-  if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  {
+    const NvtxRange r("moe_layer/router");
+    if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (!mark(1)) return MOE_ERR_CUDA;
-  if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  {
+    const NvtxRange r("moe_layer/grouping");
+    if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (!mark(2)) return MOE_ERR_CUDA;
-  if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
+  {
+    const NvtxRange r("moe_layer/experts");
+    if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (!mark(4)) return MOE_ERR_CUDA;
-  if (launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  {
+    const NvtxRange r("moe_layer/combine");
+    if (launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (!mark(5)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
