@@ -1,6 +1,7 @@
 // The C ABI of libmoe.so: host-side validation, workspace layout and the
 // enqueueing of the stage kernels. Declarations and their documentation are in
 // include/moe.h.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -10,14 +11,19 @@
 
 namespace moe {
 
+// SM count of the current device, cached per device (threads may race to fill an entry; they
+// store the same value).
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -3,20 +3,27 @@
 // once through the runtime, so libmoe.so does not link libcuda directly.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace moe {
 
+// Safe to call from several host threads: the first successful lookup is published atomically
+// (a failed one is retried on the next call).
 inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
