@@ -112,3 +112,40 @@ def test_timed_variant_rejects_bad_event_count():
     n = moe.moe_workspace_size(c)
     assert L.moe_layer_forward_timed(ctypes.byref(c), p, p, None, p, p, p, p, None, None, p, n, ev, 7,
                                      None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_fp8_quantiser_and_stats_validation_before_any_launch():
+    L = moe.lib()
+    p = 0x10000
+    c = _cfg()                                   # d_model 7168, d_ff 2048: shapes the FP8 kernels take
+    n = moe.moe_workspace_size(c)
+    ok = (p, p, p, p, p, p)                      # codes / scales of W_g, W_u, W_d
+
+    def layer(cfg, w8):
+        return L.moe_layer_forward_fp8(ctypes.byref(cfg), p, p, None, *w8, p, None, None, p, n, None)
+
+    def ffn(cfg, w8):
+        return L.moe_grouped_ffn_fp8(ctypes.byref(cfg), p, p, p, *w8, p, p, n, None)
+
+    for call in (layer, ffn):
+        assert call(c, (p, None, p, p, p, p)) == moe.MOE_ERR_INVALID_ARG          # a missing scale
+        assert call(c, (p + 8, p, p, p, p, p)) == moe.MOE_ERR_INVALID_ARG         # codes not 16-byte aligned
+        assert call(c, (p, p + 2, p, p, p, p)) == moe.MOE_ERR_INVALID_ARG         # scales not 4-byte aligned
+        assert call(_cfg(d_model=384), ok) == moe.MOE_ERR_UNSUPPORTED             # d_model not a multiple of 256
+        assert call(_cfg(d_ff=200), ok) == moe.MOE_ERR_UNSUPPORTED                # d_ff not a multiple of 128
+        assert call(_cfg(dtype="f32", d_model=256, d_ff=128), ok) == moe.MOE_ERR_UNSUPPORTED   # float32 layers
+    assert L.moe_quantize_fp8_rows(p, 4, 24, p, p, None) == moe.MOE_ERR_INVALID_ARG   # row not 16 codes wide
+    assert L.moe_quantize_fp8_rows(p, 0, 32, p, p, None) == moe.MOE_ERR_INVALID_ARG   # no rows
+    assert L.moe_quantize_fp8_rows(p + 8, 4, 32, p, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_fp8_rows(p, 4, 32, p, p + 1, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_routing_stats(ctypes.byref(c), None, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_routing_stats(ctypes.byref(c), p + 2, p, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_routing_stats(ctypes.byref(_cfg(top_k=300)), p, p, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_launch_count_follows_the_grouping_path():
+    # router, grouping (one kernel for a single 128-token chunk, else histogram, scan and
+    # scatter), the row copy, the two grouped GEMMs and the combine
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 2 + 1
+    assert moe.moe_layer_launch_count(_cfg(T=129)) == 1 + 4 + 2 + 1
+    assert moe.moe_layer_launch_count(_cfg(top_k=300)) == -1
