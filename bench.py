@@ -34,6 +34,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -172,11 +173,21 @@ GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh"),
                 "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh")}
 
 
+def code_only(src: str) -> str:
+    """C/CUDA source without its comments and blank lines (none of the hashed files has a
+    comment marker inside a string literal), so that editing comments keeps the hash."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(weights: str = "bf16") -> str:
+    """SHA-256 of the GEMM kernel's code (comments removed): a traffic capture stays valid
+    exactly as long as this is unchanged."""
     h = hashlib.sha256()
     for fn in GEMM_SOURCES[weights]:
-        with open(os.path.join(ROOT, "sparse_expert_mlp_router_b300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sparse_expert_mlp_router_b300", "csrc", fn)) as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 

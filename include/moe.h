@@ -73,7 +73,8 @@ typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_score_t;
  *   capacity_factor <= 0: dropless; > 0: each expert keeps at most
  *                   cap = ceil(capacity_factor * T * k / E) tokens, evaluated exactly on this binary32
  *                   value, admitting tokens in ascending token index; the overflow pairs contribute
- *                   nothing ("skips that expert and continues on the residual path", [ST "Load imbalance"])
+ *                   nothing: the token misses that expert and only goes on through the residual
+ *                   connection [ST "Load imbalance"]
  *   dtype           MOE_BF16 or MOE_F32 (activations and weights)
  */
 typedef struct moe_config {
@@ -162,8 +163,8 @@ moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_id
                                  cudaStream_t stream);
 
 /*
- * Grouped expert MLPs [KG definition: "grouped GEMMs on each expert's batch"; TB "Experts as
- * Specialized Subnetworks"]: for every routed expert e and kept row r in
+ * Grouped expert MLPs [KG definition: one grouped GEMM pass over every expert's batch of rows;
+ * TB "Experts as Specialized Subnetworks"]: for every routed expert e and kept row r in
  * [offsets[e], offsets[e+1]) and, for the shared expert, every token t:
  *     y = W_down (silu(W_gate a) * (W_up a)),  silu(z) = z * sigmoid(z)
  * with a = x_perm[r] (routed) or x[t] (shared). bf16: the intermediate silu(.)*(.) is

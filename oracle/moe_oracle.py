@@ -25,11 +25,11 @@ What the layer computes (the plainest reading of the pages):
                                                      [ST "The router" and its Q&A]
   5. group the (token, expert) pairs by destination expert; with a capacity
      factor cf each expert keeps at most ceil(cf * T * k / E) tokens and the
-     overflow skips that expert ("continues on the residual path")
+     overflow skips that expert (the token only goes on through the residual connection)
                                                      [KG definition; ST "Load imbalance"; ST Q&A on capacity factor]
   6. each kept pair runs its expert's MLP; the MLP form is not fixed by the
-     pages ("a standard feedforward block", TB "Experts as Specialized
-     Subnetworks"); this layer uses SwiGLU without biases:
+     pages (each expert is only called an ordinary feed-forward block, TB "Experts as
+     Specialized Subnetworks"); this layer uses SwiGLU without biases:
         y = W_down (silu(W_gate x) * (W_up x)),  silu(z) = z / (1 + exp(-z))
   7. out[t] = sum over the token's kept slots j of g_j * y_j, plus every shared
      expert's MLP of x[t] with weight one           [ST "The router" (shared experts); KG definition]

@@ -6,8 +6,8 @@
 // a top-k router work?" (the output is the gate-weighted sum of the selected
 // experts' outputs) and section "The router" (shared experts every token
 // visits), and klaylearn.com/glossary/mixture-of-experts (undo the
-// permutation). A dropped slot (dest_row = -1) contributes nothing: the token
-// "continues on the residual path" for that expert (same page, "Load
+// permutation). A dropped slot (dest_row = -1) contributes nothing: for that
+// expert the token only goes on through the residual connection (same page, "Load
 // imbalance"); the residual add itself is outside this layer.
 //
 // One CTA per token; each thread owns 16 bytes of the row and accumulates its

@@ -1,8 +1,8 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
 // fed by TMA over a per-expert tile schedule.
 //
-// "Permuting tokens by destination expert, running grouped GEMMs on each
-// expert's batch, then undoing the permutation" (klaylearn.com/glossary/
+// The MoE layer sorts tokens by the expert they go to, multiplies each expert's
+// batch in grouped GEMMs and restores token order afterwards (klaylearn.com/glossary/
 // mixture-of-experts, "Mixture of Experts", definition). The expert is a SwiGLU
 // MLP y = W_down (silu(W_gate a) * (W_up a)); this file holds its two
 // contractions:

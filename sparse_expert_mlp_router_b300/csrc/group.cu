@@ -1,13 +1,12 @@
 // Grouping of (token, slot) pairs by destination expert: histogram, prefix sum,
 // capacity, scatter of row indices, and the 16-byte row gather of x.
 //
-// Follows klaylearn.com/glossary/mixture-of-experts "Mixture of Experts" (the
-// definition: "permuting tokens by destination expert, running grouped GEMMs on
-// each expert's batch, then undoing the permutation") and
-// shubhamtatvamasi.com/llm-inference/moe "Mixture of Experts", section "Load
-// imbalance" (each expert accepts at most capacity factor x ideal tokens, the
-// overflow skips that expert; or dropless) and its Q&A on capacity factor
-// ("factor x (T.k/E) tokens").
+// Follows klaylearn.com/glossary/mixture-of-experts "Mixture of Experts" (its
+// definition: tokens are sorted by the expert they go to before the grouped GEMMs,
+// and put back in order after) and shubhamtatvamasi.com/llm-inference/moe "Mixture
+// of Experts", section "Load imbalance" (each expert accepts at most the capacity
+// factor times its even share of the tokens, the overflow skips that expert; or
+// dropless) and its Q&A on capacity factor (the even share is T·k/E).
 //
 // Determinism: within one expert, rows follow ascending token index, and the
 // tokens past the capacity are the highest-index ones. The kernels reach this

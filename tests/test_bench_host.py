@@ -92,3 +92,12 @@ def test_clock_samples_parse_throttle_reasons_and_medians():
 def test_whole_job_rate_counts_every_rank():
     assert bench.whole_job_rate(4096, 100, 1, 1000.0) == pytest.approx(409600.0)
     assert bench.whole_job_rate(4096, 100, 8, 1000.0) == pytest.approx(8 * 409600.0)
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    src = "// header\nint f(int a) {\n  return a + 1;  // one\n}\n/* block\n comment */\n"
+    recommented = "// another header\n\nint f(int a) {\n  return a + 1;\n}\n"
+    changed = "// header\nint f(int a) {\n  return a + 2;  // one\n}\n"
+    assert bench.code_only(src) == bench.code_only(recommented)
+    assert bench.code_only(src) != bench.code_only(changed)
+    assert len(bench.kernel_source_hash("bf16")) == 64
