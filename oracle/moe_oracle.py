@@ -196,7 +196,7 @@ def combine(dest_row: np.ndarray, gate: np.ndarray, y_rows: np.ndarray,
     """out[t] = sum over kept slots of gate * expert output, plus the shared part.
 
     [ST Q&A "How does a top-k router work?": gate-weighted sum; ST "The router":
-    shared experts every token always visits.] Dropped slots add nothing.
+    shared experts, which all tokens pass through.] Dropped slots add nothing.
     """
     T, k = dest_row.shape
     out = np.zeros((T, d_model), dtype=np.float64)

@@ -3,9 +3,9 @@
 //
 // The schedule turns the kept-pair offsets of the grouping stage into the
 // per-group row ranges and 128-row tile counts the grouped GEMMs walk (one
-// group per routed expert, then one per shared expert: "shared experts that
-// every token always visits", shubhamtatvamasi.com/llm-inference/moe "Mixture
-// of Experts", section "The router"). It also checks the offsets: a grouping
+// group per routed expert, then one per shared expert, which all tokens pass
+// through: shubhamtatvamasi.com/llm-inference/moe "Mixture of Experts", section
+// "The router"). It also checks the offsets: a grouping
 // that is not monotone or overruns the row capacity is recorded as
 // MOE_ERR_DEVICE_INDEX and replaced by an empty one, so no kernel reads out of
 // bounds.
