@@ -1,29 +1,36 @@
 #!/usr/bin/env python
 """Benchmark of the MoE FFN layer forward on B300: prints ONE JSON line (rank 0).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--extra-workloads LIST]
+                    [--impl ours|reference]
 
 A step is one moe_layer_forward over one batch of synthetic input (router ->
-grouping -> grouped SwiGLU GEMMs -> combine). Default workload: the
-Mixtral-8x7B-shaped prefill layer (T=4096, d=4096, 8 experts, top-2, d_ff=14336).
+grouping -> grouped SwiGLU GEMMs -> combine). The headline workload (the line's
+own keys) is the Mixtral-8x7B-shaped prefill layer (T=4096, d=4096, 8 experts,
+top-2, d_ff=14336); the other four model-shaped layers (Qwen3-30B-A3B-shaped,
+DeepSeek-V3-shaped with capacity drops and a shared expert, the decode-shaped
+batch of 32 tokens, the tiny float32 layer) are measured the same way in the same
+run and reported under "workloads", one entry each.
 
-value        tokens/s with inputs resident in HBM, K steps timed with CUDA events
-             (barrier + synchronize on both sides, max over ranks); expert weights
-             (2.8 GB) exceed the 126 MB L2, so every step streams them from HBM.
-             The K moe_layer_forward calls are captured into one CUDA graph and
-             replayed (--eager: K separate calls); each captured call enqueues the
-             same kernels as an eager one. Stage times (and the roofline's kernel
-             time) come from a second replay of the same K calls with CUDA events
-             at the stage boundaries (--eager: from the timed calls themselves).
+value        tokens/s with inputs resident in HBM: K steps timed with CUDA events
+             (barrier + synchronize on both sides, max over ranks); the expert
+             weights exceed the 126 MB L2, so every step streams them from HBM.
+             The K moe_layer_forward calls run as CUDA-graph replays of plain layer
+             calls, in four chunks; after each timed chunk the same calls replay with
+             CUDA events at the stage boundaries (untimed for `value`), so the stage
+             times and the layer time are taken under the same clocks and power.
+             --eager: K separate calls with the stage events, timed as they run.
 e2e          the same metric through the same C-ABI call with the activations in
              pinned host memory: each step copies x host->device, runs the layer and
              copies out device->host. Steps with at least 1 MB of activations run their
              copies on their own streams, overlapping the neighbouring steps' layers;
              smaller steps run serially on one stream. Both loops are reported.
 roofline     the dominant kernel (the gate/up grouped GEMM), timed by events recorded
-             around it on the launching stream, in the staged replay of the K layers.
-cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload.
---impl reference  times that oracle alone, step by step, on the host cores.
+             around it on the launching stream, in the staged replays.
+cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload: the whole
+             batch's routing and grouping, the expert MLPs and combine of a token sample.
+--impl reference  times that oracle alone on the host cores, step by step, each step
+             the same kind of bounded sample of the headline workload.
 N > 1 (torchrun): every rank runs its own replica of the layer (the layer has no
 exchange step), value = all ranks' tokens / max time.
 """
@@ -49,30 +56,54 @@ UNIT = "tokens/s"
 OVERLAP_MIN_BYTES = 1 << 20          # end-to-end loop: overlap the copies from this size
 E2E_WARM_S = 0.3                     # end-to-end loops: warm-up wall time
 E2E_MIN_S = 0.3                      # end-to-end loops: least timed device time
+TIMED_CHUNKS = 4                     # plain / staged replay pairs the K timed steps are split into
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+HEADLINE = "mixtral_8x7b"
+EXTRA_WORKLOADS = ("qwen3_30b_a3b", "deepseek_v3", "decode_qwen3", "tiny_f32")
+# tokens whose expert MLPs the CPU oracle runs (the routing and grouping always cover the whole
+# batch); sized for a few seconds of fp64 work each, weights generated outside the timing
+CPU_SAMPLE_TOKENS = {"mixtral_8x7b": 2048, "qwen3_30b_a3b": 512, "deepseek_v3": 16, "decode_qwen3": 32,
+                     "tiny_f32": 64}
+REF_TOKENS_PER_STEP = {"mixtral_8x7b": 64, "qwen3_30b_a3b": 64, "deepseek_v3": 2, "decode_qwen3": 32,
+                       "tiny_f32": 64}
+# float32 FMA rate of the CUDA cores: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
+F32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="mixtral_8x7b")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--extra-workloads", default=None,
+                    help="comma-separated workloads measured after the headline one and reported under "
+                         "'workloads' (default: the other four model-shaped layers when the headline is "
+                         f"{HEADLINE}, none otherwise; 'none' for none)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="end-to-end steps per loop (default: at least 100 and 0.3 s of layers)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=None,
+                    help="tokens whose expert MLPs the CPU oracle runs (default: per workload)")
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales")
     ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
                     help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
                          "write_traffic) and exit")
     ap.add_argument("--eager", action="store_true",
-                    help="time K separate launches of the layer instead of one CUDA-graph replay of K layers")
-    return ap.parse_args()
+                    help="time K separate launches of the layer instead of CUDA-graph replays")
+    return ap.parse_args(argv)
+
+
+def extra_workloads(args) -> list:
+    if args.extra_workloads is None:
+        return list(EXTRA_WORKLOADS) if args.workload == HEADLINE and args.gpus == 1 else []
+    if args.extra_workloads.strip().lower() in ("", "none"):
+        return []
+    return [n.strip() for n in args.extra_workloads.split(",") if n.strip() and n.strip() != args.workload]
 
 
 # ----------------------------------------------------------------- helpers
@@ -95,18 +126,21 @@ def load_peaks():
 
 def algorithmic(w, kept_pairs: int, groups_touched: int, weight_bytes: float = 2.0):
     """Work of one layer forward, from the realised routing (counted, not estimated).
-    weight_bytes: bytes per stored expert weight (2 for bf16, 1 for FP8 codes, whose per-row
-    float32 scales are counted too)."""
+    weight_bytes: bytes per stored expert weight (2 for bf16, 4 for float32, 1 for FP8 codes,
+    whose per-row float32 scales are counted too). Activations are bf16 (float32 layers: 4 bytes)."""
     rows = kept_pairs + w.n_shared * w.T
     d, F = w.d_model, w.d_ff
-    e = 2  # bytes per bf16 activation
+    e = 2 if w.dtype == "bf16" else 4   # bytes per activation
     scales = 4.0 if weight_bytes < 2 else 0.0
+    gu_w = groups_touched * 2.0 * F * (d * weight_bytes + scales)
+    dn_w = groups_touched * 1.0 * d * (F * weight_bytes + scales)
     return {
         "gateup_flops": 4.0 * d * F * rows,
         "down_flops": 2.0 * d * F * rows,
         "router_flops": 2.0 * w.T * d * w.n_experts,
-        "gateup_bytes": groups_touched * 2.0 * F * (d * weight_bytes + scales) + rows * d * e + rows * F * e,
-        "down_bytes": groups_touched * 1.0 * d * (F * weight_bytes + scales) + rows * F * e + rows * d * e,
+        "gateup_bytes": gu_w + rows * d * e + rows * F * e,
+        "down_bytes": dn_w + rows * F * e + rows * d * e,
+        "weight_bytes": gu_w + dn_w,
     }
 
 
@@ -252,52 +286,122 @@ def cpu_threads() -> int:
     return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def config_of(w, kept: int, touched: int, world: int, weights: str) -> dict:
+    """The `config` object of a bench line: what the workload is, identical in both arms."""
+    fp8 = weights == "fp8"
+    return {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
+            "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff, "score": w.score,
+            "renormalize": bool(w.renormalize), "capacity_factor": w.capacity_factor, "kept_pairs": int(kept),
+            "groups_touched": int(touched),
+            "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step"
+                  % (touched * 3.0 * w.d_model * w.d_ff * (1 if fp8 else (2 if w.dtype == "bf16" else 4)) / 1e9)
+                  if touched * 3.0 * w.d_model * w.d_ff * 2 > 126e6 else
+                  "inputs smaller than L2 (%.1f MB of expert weights): a latency-bound layer"
+                  % (touched * 3.0 * w.d_model * w.d_ff * (2 if w.dtype == "bf16" else 4) / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "weights": "fp8 e4m3, per-row float32 scales" if fp8 else w.dtype}
+
+
 # ----------------------------------------------------------- the CPU oracle
 
-def oracle_sample(w, n_tokens: int, one_token_batches: bool):
-    """Returns (callable that runs the oracle once, tokens it covers, description).
+class OracleSample:
+    """The fp64 oracle's layer forward on a bounded sample of a workload.
 
-    The expert weights are generated on the host and converted to float64 before the
-    timing starts; the timed call is the oracle's layer forward alone.
+    Each call routes and groups the whole batch (admission under a capacity limit depends on
+    the whole batch) and runs the expert MLPs and the combine for `n_tokens` tokens of it.
+    Expert weights are generated on the host and converted to float64 either once before any
+    timing (`preload`, when they fit in `max_cached_bytes`) or on demand, one expert at a
+    time; the time spent generating them is measured and excluded from the oracle's time.
     """
-    import numpy as np
-    import oracle as O
-    import synth
 
-    x64 = synth.as_f64(synth.host_tensor(w, "x"), w.dtype)
-    wr64 = synth.as_f64(synth.host_tensor(w, "w_router"), w.dtype)
-    bias = synth.router_bias(w.n_experts, w.bias_s)
-    rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(w.T, size=min(n_tokens, w.T), replace=False))
-    if one_token_batches:
-        assert w.capacity_factor <= 0, "a one-token batch changes capacity; use a dropless workload"
+    def __init__(self, w, n_tokens: int, seed: int = 0, max_cached_bytes: float = 24e9):
+        import numpy as np
+        import oracle as O
+        import synth
+        self.w, self.O, self.synth, self.np = w, O, synth, np
+        self.x64 = synth.as_f64(synth.host_tensor(w, "x"), w.dtype)
+        self.wr64 = synth.as_f64(synth.host_tensor(w, "w_router"), w.dtype)
+        self.bias = synth.router_bias(w.n_experts, w.bias_s)
+        self.n = max(1, min(n_tokens, w.T))
+        self.rng = np.random.default_rng(seed)
+        self.kw = dict(top_k=w.top_k, score=w.score, renormalize=w.renormalize,
+                       capacity_factor=w.capacity_factor, n_shared=w.n_shared)
+        self.gen_s = 0.0
+        self.cache = {}
+        self.per_expert = 3.0 * w.d_model * w.d_ff * 8
+        self.max_cached = max_cached_bytes
+        self.lazy = True
+
+    def preload(self, token_sets) -> None:
+        """Generate before timing the experts the given token sets will touch, if they fit."""
+        np, O = self.np, self.O
+        idx, _, _ = O.route(self.x64, self.wr64, self.bias, self.w.top_k, self.w.score, self.w.renormalize)
         need = set()
-        idx, _, _ = O.route(x64[toks], wr64, bias, w.top_k, w.score, w.renormalize)
-        need |= set(np.unique(idx).tolist())
-    else:
-        idx, _, _ = O.route(x64, wr64, bias, w.top_k, w.score, w.renormalize)
-        need = set(np.unique(idx[toks]).tolist())
-    need |= set(range(w.n_experts, w.n_experts + w.n_shared))
-    cache = {g: tuple(synth.as_f64(a, w.dtype) for a in synth.host_expert(w, g)) for g in sorted(need)}
-    experts = cache.__getitem__
-    kw = dict(top_k=w.top_k, score=w.score, renormalize=w.renormalize, capacity_factor=w.capacity_factor,
-              n_shared=w.n_shared)
-    if one_token_batches:
-        state = {"i": 0}
+        for toks in token_sets:
+            need |= set(np.unique(idx[toks]).tolist())
+        need |= set(range(self.w.n_experts, self.w.n_experts + self.w.n_shared))
+        if len(need) * self.per_expert > self.max_cached:
+            return
+        for g in sorted(need):
+            self.cache[g] = self._gen(g)
+        self.lazy = False
 
-        def run():
-            t = toks[state["i"] % len(toks)]
-            state["i"] += 1
-            O.layer_forward(x64[t:t + 1], wr64, bias, experts, **kw)
-            return 1
-        desc = f"{w.name}: one token per step (a 1-token dropless batch), tokens drawn from the {w.T}-token batch"
+    def _gen(self, g):
+        return tuple(self.synth.as_f64(a, self.w.dtype) for a in self.synth.host_expert(self.w, g))
+
+    def experts(self, g):
+        if g in self.cache:
+            return self.cache[g]
+        t0 = time.perf_counter()
+        if self.lazy:
+            self.cache.clear()
+        v = self.cache[g] = self._gen(g)
+        self.gen_s += time.perf_counter() - t0
+        return v
+
+    def draw(self):
+        return self.np.sort(self.rng.choice(self.w.T, size=self.n, replace=False))
+
+    def run(self, toks) -> tuple:
+        """One oracle layer forward restricted to `toks`; returns (tokens, oracle seconds)."""
+        g0 = self.gen_s
+        t0 = time.perf_counter()
+        self.O.layer_forward(self.x64, self.wr64, self.bias, self.experts, tokens=toks, **self.kw)
+        dt = time.perf_counter() - t0 - (self.gen_s - g0)
+        return len(toks), dt
+
+    def describe(self, steps: int = 1) -> str:
+        per = f"expert MLPs and combine of {self.n} sampled tokens" + (" per step" if steps > 1 else "")
+        return (f"{self.w.name}: routing and grouping of the whole {self.w.T}-token batch, {per}; "
+                f"weight generation excluded")
+
+
+def cpu_baseline(w, n_tokens: int, one_core: bool = False) -> dict:
+    """The oracle timed once on a bounded sample of workload w (all host cores, or one)."""
+    s = OracleSample(w, n_tokens)
+    toks = s.draw()
+    s.preload([toks])
+    if one_core:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            n, dt = s.run(toks)
+        cores = 1
     else:
-        def run():
-            O.layer_forward(x64, wr64, bias, experts, tokens=toks, **kw)
-            return len(toks)
-        desc = (f"{w.name}: routing and grouping of all {w.T} tokens, expert MLPs and combine for "
-                f"{len(toks)} sampled tokens")
-    return run, desc
+        n, dt = s.run(toks)
+        cores = cpu_threads()
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": s.describe(),
+            "seconds": dt, "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def max_over_ranks(ms: float, dist=None, device="cuda") -> float:
@@ -316,25 +420,36 @@ def whole_job_rate(tokens_per_step: int, steps: int, world: int, max_ms: float) 
 
 
 def run_reference(args, w):
+    """The reference arm: the fp64 oracle alone on the host cores. Each step is one oracle layer
+    forward over the whole batch's routing and grouping with the expert MLPs and combine of a
+    fresh token sample, as in the CPU baseline; value = sampled tokens / oracle time."""
+    import numpy as np
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    run, desc = oracle_sample(w, max(args.steps + args.warmup, 1), one_token_batches=True)
-    for _ in range(args.warmup):
-        run()
-    t0 = time.perf_counter()
-    n = 0
-    for _ in range(args.steps):
-        n += run()
-    dt = time.perf_counter() - t0
-    value = n / dt
+    n_tok = args.cpu_sample_tokens or REF_TOKENS_PER_STEP.get(w.name, 64)
+    s = OracleSample(w, n_tok)
+    samples = [s.draw() for _ in range(args.warmup + args.steps)]
+    s.preload(samples)
+    for i in range(args.warmup):
+        s.run(samples[i])
+    n, dt = 0, 0.0
+    for i in range(args.steps):
+        a, b = s.run(samples[args.warmup + i])
+        n, dt = n + a, dt + b
+    value = n / dt if dt > 0 else 0.0
+    idx, _, _ = s.O.route(s.x64, s.wr64, s.bias, w.top_k, w.score, w.renormalize)
+    counts = np.bincount(idx.ravel(), minlength=w.n_experts)
+    cap = s.O.capacity(w.T, w.top_k, w.n_experts, w.capacity_factor)
+    kept_e = counts if cap is None else np.minimum(counts, cap)
+    kept, touched = int(kept_e.sum()), int((kept_e > 0).sum()) + w.n_shared
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
-                   "top_k": w.top_k, "d_ff": w.d_ff},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc},
+        "config": config_of(w, kept, touched, 1, args.weights),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": s.describe(args.steps), "cpu_model": cpu_model(), "nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -342,18 +457,20 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------- our layer
 
-def run_ours(args, w):
+def chunk_sizes(K: int, n: int = TIMED_CHUNKS) -> list:
+    """K steps split into at most n chunks of at most two sizes (largest first)."""
+    n = max(1, min(n, K))
+    base, extra = divmod(K, n)
+    return [base + 1] * extra + [base] * (n - extra)
+
+
+def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
+    """Everything the bench reports for one workload: device-timed value, stage times, roofline,
+    end-to-end rate, clocks and (rank 0, N = 1) the CPU oracle baseline."""
     import numpy as np
     import torch
     import synth
     import sparse_expert_mlp_router_b300 as moe
-
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     def barrier():
         if dist is not None:
@@ -364,7 +481,7 @@ def run_ours(args, w):
                           n_shared=w.n_shared, score=w.score, renormalize=w.renormalize,
                           capacity_factor=w.capacity_factor, dtype=w.dtype)
     dev = synth.device_inputs(w)
-    fp8 = args.weights == "fp8"
+    fp8 = args.weights == "fp8" and w.dtype == "bf16"
     if fp8:
         # FP8 codes and per-row scales made on the device by the library's quantiser; the bf16
         # copies are freed before any timing
@@ -388,37 +505,41 @@ def run_ours(args, w):
     forward(*args_fwd, counts_out=counts)
     status = moe.moe_get_device_error(ws)
     if status != moe.MOE_OK:
-        raise RuntimeError(f"device status {moe.status_string(status)}")
+        raise RuntimeError(f"{w.name}: device status {moe.status_string(status)}")
     cap = moe.moe_capacity(cfg)
     c = counts.cpu().numpy()
     kept = int(np.minimum(c, cap).sum())
     touched = int((np.minimum(c, cap) > 0).sum()) + w.n_shared
-    work = algorithmic(w, kept, touched, 1.0 if fp8 else 2.0)
+    work = algorithmic(w, kept, touched, 1.0 if fp8 else (2.0 if w.dtype == "bf16" else 4.0))
 
     K, W = args.steps, args.warmup
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    sizes = chunk_sizes(K) if not args.eager else [K]
+    n_ev = max(sizes)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_ev)]
     for row in evs:            # create every event before any capture
         for e in row:
             e.record()
     for i in range(W):
-        forward_timed(*args_fwd, evs[i % K])
+        forward_timed(*args_fwd, evs[i % n_ev])
     barrier()
-    # Graph mode: the timed region replays K plain moe_layer_forward calls; the stage times come
-    # from a second replay of the same K calls with CUDA events recorded at the stage boundaries
-    # (six event records a layer cost the decode-shaped layer about 8 %). Eager mode (--eager,
-    # for profilers): K calls with the stage events, timed as they run.
-    graph = graph_staged = None
+    # Graph mode: the K timed steps are CUDA-graph replays of plain moe_layer_forward calls in
+    # TIMED_CHUNKS chunks; after each timed chunk the same number of calls replays with CUDA
+    # events at the five stage boundaries (six event records a layer cost the decode-shaped
+    # layer about 8 %, so they stay out of the timed replays). Alternating the two keeps the
+    # stage times under the same clocks and power as the timed layers.
+    plain, staged = {}, {}
     if not args.eager:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for i in range(K):
-                forward(*args_fwd)
-        graph_staged = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_staged):
-            for i in range(K):
-                forward_timed(*args_fwd, evs[i])
-        graph.replay()         # one untimed replay of each
-        graph_staged.replay()
+        for n in sorted(set(sizes)):
+            plain[n] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(plain[n]):
+                for i in range(n):
+                    forward(*args_fwd)
+            staged[n] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(staged[n]):
+                for i in range(n):
+                    forward_timed(*args_fwd, evs[i])
+            plain[n].replay()      # one untimed replay of each
+            staged[n].replay()
         barrier()
     props = torch.cuda.get_device_properties(local)
     try:
@@ -427,28 +548,33 @@ def run_ours(args, w):
         gpu_id = str(local)
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record()
-    if graph is not None:
-        graph.replay()
-    else:
-        for i in range(K):
-            forward_timed(*args_fwd, evs[i])
-    t_end.record()
-    barrier()
-    if graph_staged is not None:
-        graph_staged.replay()
+    elapsed_ms = 0.0
+    stage_rows = []
+    for n in sizes:
         barrier()
+        t_start.record()
+        if args.eager:
+            for i in range(n):
+                forward_timed(*args_fwd, evs[i])
+        else:
+            plain[n].replay()
+        t_end.record()
+        barrier()
+        elapsed_ms += t_start.elapsed_time(t_end)
+        if not args.eager:
+            staged[n].replay()
+            torch.cuda.synchronize()
+        stage_rows += [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(n)]
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])   # [K, 5] ms
+    stage = np.array(stage_rows)       # [K, 5] ms
     status = moe.moe_get_device_error(ws)
     if status != moe.MOE_OK:
-        raise RuntimeError(f"device status after timing: {moe.status_string(status)}")
+        raise RuntimeError(f"{w.name}: device status after timing: {moe.status_string(status)}")
     max_ms = max_over_ranks(elapsed_ms, dist)
     value = whole_job_rate(w.T, K, world, max_ms)
+    del plain, staged
 
     # end to end: activations in pinned host memory, copies inside the timed region. Two loops:
     # serial (one stream: copy x in, run the layer, copy the output out), and overlapped (the
@@ -524,59 +650,49 @@ def run_ours(args, w):
     overlapped = x_host.numel() * x_host.element_size() >= OVERLAP_MIN_BYTES
     e2e_value = whole_job_rate(w.T, K2, world, overlap_ms if overlapped else serial_ms)
     if moe.moe_get_device_error(ws) != moe.MOE_OK:
-        raise RuntimeError("device status after e2e timing")
+        raise RuntimeError(f"{w.name}: device status after e2e timing")
 
     # roofline of the dominant kernel: the gate/up grouped GEMM (stage 2 -> 3). A tensor-bound
     # kernel timed inside a long run of back-to-back layers (>= 1 s, where the GPU settles at
     # its power limit) is compared with the sustained bf16 rate, else with the burst rate; the
-    # fraction of the burst rate is reported as well.
+    # fraction of the burst rate is reported as well. The float32 layer's MLP runs on the CUDA
+    # cores and is compared with their FMA rate.
     peaks, peak_src = load_peaks()
     gemm_ms = float(stage[:, 2].mean())
-    t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * 1e12)
-    t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    pair_ms = float((stage[:, 2] + stage[:, 3]).mean())
     long_run = max_ms >= 1000.0
-    if t_tensor >= t_bytes:
+    if w.dtype != "bf16":
         achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac_of_burst": achieved / peaks["bf16_tflops"]}
+        roof = {"bound": "alu", "achieved": achieved, "peak": F32_FMA_TFLOPS, "unit": "TFLOP/s",
+                "kernel": "ffn_gateup_fma_kernel (float32, CUDA cores)",
+                "peak_source": "float32 FMA rate: 148 SMs x 128 lanes x 2 flops x 2.032 GHz"}
     else:
-        achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
+        if t_tensor >= t_bytes:
+            achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
+            peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac_of_burst": achieved / peaks["bf16_tflops"]}
+        else:
+            achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof["kernel"] = ("grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
+                          "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
+        roof["peak_source"] = (f"{peak_src} copy bandwidth" if roof["bound"] == "hbm" else
+                               f"{peak_src} sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else
+                               f"{peak_src} burst")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.name, args.weights)
-    roof["kernel"] = ("grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
-                      "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
-    roof["peak_source"] = (f"{peak_src} copy bandwidth" if roof["bound"] == "hbm" else
-                           f"{peak_src} sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else
-                           f"{peak_src} burst")
+    roof["traffic"] = measured_traffic(w.name, "fp8" if fp8 else "bf16") if w.dtype == "bf16" else None
     roof["ms_per_launch"] = gemm_ms
 
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
                          [float(v) for v in stage.mean(axis=0)]))
-    gemm_tflops = (work["gateup_flops"] + work["down_flops"]) / ((stage[:, 2] + stage[:, 3]).mean() / 1e3) / 1e12
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        run, desc = oracle_sample(w, args.cpu_sample_tokens, one_token_batches=False)
-        t0 = time.perf_counter()
-        n = run()
-        dtc = time.perf_counter() - t0
-        cpu = {"value": n / dtc, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": desc,
-               "seconds": dtc}
-
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": max_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
-                   "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff, "score": w.score,
-                   "capacity_factor": w.capacity_factor, "kept_pairs": kept, "groups_touched": touched,
-                   "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step"
-                         % (touched * 3.0 * w.d_model * w.d_ff * 2 / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": "eager" if args.eager else "cuda_graph",
-                   "weights": "fp8 e4m3, per-row float32 scales" if fp8 else w.dtype},
+    pair_flops = work["gateup_flops"] + work["down_flops"]
+    weight_bytes = work["weight_bytes"]
+    res = {
+        "value": value, "ms_per_step": max_ms / K, "steps": K,
+        "config": config_of(w, kept, touched, world, "fp8" if fp8 else "bf16"),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": K2,
                 "copies": ("own streams, overlapping the neighbouring steps' layers (double-buffered)"
@@ -586,11 +702,54 @@ def run_ours(args, w):
                 "overlapped_value": whole_job_rate(w.T, K2, world, overlap_ms)},
         "gpu_launches": K * moe.moe_layer_launch_count(cfg),
         "roofline": roof,
-        "cpu_baseline": cpu,
         "clocks": clocks,
         "stages_ms": stages_ms,
-        "grouped_gemm_tflops": gemm_tflops,
+        "stages_sum_ms": float(stage.sum(axis=1).mean()),
+        "grouped_gemm_tflops": pair_flops / (pair_ms / 1e3) / 1e12,
+        "grouped_gemm_frac_of_burst": pair_flops / (pair_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "expert_weight_gbs": weight_bytes / (pair_ms / 1e3) / 1e9,
+        "expert_weight_frac_of_hbm": weight_bytes / (pair_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
     }
+    del dev, ws, out, counts, x_host, out_hosts, x_devs, out_devs, wargs, args_fwd
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if with_cpu:
+        n = args.cpu_sample_tokens or CPU_SAMPLE_TOKENS.get(w.name, 256)
+        res["cpu_baseline"] = cpu_baseline(w, n)
+        if w.name == "tiny_f32":
+            res["cpu_baseline"]["one_core"] = cpu_baseline(w, n, one_core=True)
+    else:
+        res["cpu_baseline"] = None
+    return res
+
+
+def run_ours(args, w):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head = measure_workload(args, w, dist, local, rank, world, with_cpu)
+    extras = {}
+    for name in extra_workloads(args):
+        import synth
+        extras[name] = measure_workload(args, synth.WORKLOADS[name], dist, local, rank, world, with_cpu)
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": head["config"], "launch": "eager" if args.eager else "cuda_graph",
+        "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
+        "cpu_baseline": head["cpu_baseline"], "clocks": head["clocks"], "stages_ms": head["stages_ms"],
+        "stages_sum_ms": head["stages_sum_ms"], "grouped_gemm_tflops": head["grouped_gemm_tflops"],
+        "grouped_gemm_frac_of_burst": head["grouped_gemm_frac_of_burst"],
+        "expert_weight_frac_of_hbm": head["expert_weight_frac_of_hbm"],
+    }
+    if extras:
+        line["workloads"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -147,14 +147,18 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  * device memory and passes in only the call's tensors, a real-time loop that must not touch
  * the allocator. The source pages have no counterpart; this is an interface of this library.
  *   Same arguments and results as moe_permute, without ws / ws_bytes, plus
- *   status  device int32 or NULL: a device-side problem (an id outside [0, E)) is recorded
- *           here with an atomic compare-and-swap from 0, so zero it before the call.
- * The per-chunk expert histogram lives in a fixed 256 KiB array in libmoe.so's own device
- * memory, held by every GPU that loads the library until the process exits. It fits
- * ceil(T/128) * E <= 65536 (T <= 32768 at E = 256); larger configurations return
- * MOE_ERR_WORKSPACE before anything is enqueued. Nothing is allocated or freed. The first
- * call on a device looks up the array's device address: make it before any stream capture.
- * All calls share the array and leave their contents in it; calls that overlap on the GPU
+ *   status  device int32 or NULL: a device-side problem (an id outside [0, E), or an expert
+ *           repeated within a token) is recorded here with an atomic compare-and-swap from 0,
+ *           so zero it before the call. With status == NULL such problems go unreported: the
+ *           pair is still skipped (dest_row = -1) but nothing records that it happened.
+ * Batches of at most 128 tokens are grouped by one CTA in its own shared memory and touch no
+ * shared state. Larger batches keep the per-chunk expert histogram in a fixed 256 KiB array in
+ * libmoe.so's own device memory, held by every GPU that loads the library until the process
+ * exits. It fits ceil(T/128) * E <= 65536 (T <= 32768 at E = 256); larger configurations
+ * return MOE_ERR_WORKSPACE before anything is enqueued. Nothing is allocated or freed. The
+ * first such call in a CUDA context looks up the array's device address (again after a
+ * cudaDeviceReset or under another context): make it before any stream capture. All these
+ * calls share the array and leave their contents in it; calls that overlap on the GPU
  * (unordered streams) race and give wrong results.
  */
 moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_idx, const void* x,
@@ -218,6 +222,10 @@ moe_status_t moe_grouped_ffn_fp8(const moe_config_t* cfg, const void* x_perm, co
  * accumulated in float32 in slot order, shared part last. No residual add.
  *   y_perm device [R + S*T, d_model] in; dest_row device [T, k] int32; topk_gate device [T, k] float32
  *   out    device [T, d_model] out
+ *   ws, ws_bytes  the workspace (moe_workspace_size bytes, 256-byte aligned): only its status
+ *          word is used, to record a dest_row entry at or past R (the entry is then skipped).
+ * The per-expert offsets of the grouping are not an argument: dest_row already names each
+ * pair's grouped row (or -1), and the shared expert's rows follow the R routed rows.
  */
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* dest_row,
                          const float* topk_gate, void* out, void* ws, size_t ws_bytes,

@@ -63,7 +63,7 @@ import numpy as np
 __all__ = [
     "router_logits", "scores_from_logits", "select_topk", "gates_from_scores", "route",
     "capacity", "dispatch", "silu", "expert_mlp", "combine", "layer_forward", "LayerResult",
-    "flops_per_pair", "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
+    "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
     "routing_stats", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "dequantize_fp8_rows",
 ]
 
@@ -278,11 +278,6 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
 
 # ---------------------------------------------------------------------------
 # accounting rules the pages state
-
-def flops_per_pair(d_model: int, d_ff: int) -> int:
-    """Multiply-adds of one SwiGLU expert on one token, counted as 2 flops each: 3 matrices of d x F."""
-    return 6 * d_model * d_ff
-
 
 def flops_per_token(active_params: float) -> float:
     """FLOPs per token = 2 x active parameters [ST "Memory vs compute, quantified", table]."""

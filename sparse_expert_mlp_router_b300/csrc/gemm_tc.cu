@@ -84,6 +84,7 @@ struct GemmArgs {
   __nv_bfloat16* out;
   int64_t ldo;          // elements per output row
   int32_t* status;
+  int b_evict_first;    // load B (the weights) with an L2 evict-first policy
 };
 
 // Epilogue of one accumulator row (this thread's TMEM lane): output columns
@@ -216,6 +217,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0;
       int issued = 0;              // loads issued (saturating at kStages)
       bool ok = true;
+      const uint64_t b_policy = ptx::l2_policy_evict_first();
       for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
         int g, m, n;
         decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
@@ -232,8 +234,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sb = sa + C::kABytes;
           ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
           ptx::tma_load_2d(sa, use_a2 ? (const void*)&tmA2 : (const void*)&tmA, kb * kBK, a_row, fb);
-          ptx::tma_load_2d(sb, &tmB, kb * kBK, b_row, fb);
-          if (MODE == 0) ptx::tma_load_2d(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb);
+          if (args.b_evict_first) {
+            ptx::tma_load_2d_hint(sb, &tmB, kb * kBK, b_row, fb, b_policy);
+            if (MODE == 0) ptx::tma_load_2d_hint(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb, b_policy);
+          } else {
+            ptx::tma_load_2d(sb, &tmB, kb * kBK, b_row, fb);
+            if (MODE == 0) ptx::tma_load_2d(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb);
+          }
           if (issued < C::kStages) ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -583,6 +590,21 @@ bool pairs_fit(const cudaLaunchConfig_t& cfg) {
 // few percent of the single-CTA kernel on the tensor-bound layers (all of them run at the
 // power limit) and slower where experts have few rows (decode, capacity-limited layers),
 // where a 256-row tile doubles the wasted MMA work.
+// Whether the weights (B) of a grouped GEMM are loaded with the L2 evict-first policy. The
+// m-tiles that read one weight tile run in the same wave, so the weights need L2 only briefly,
+// while the activation rows (A) are read again by later waves for the other n-tiles: with
+// evict-first on the weights, L2 keeps the activations. Default: on for the down projection
+// (K = d_ff is long, so an expert's h rows are the larger reuse set), off for gate/up;
+// MOE_GEMM_B_EVICT_FIRST=0/1 (read once per process) sets both.
+int b_evict_first(int mode) {
+  static const int forced = [] {
+    const char* v = getenv("MOE_GEMM_B_EVICT_FIRST");
+    return v == nullptr ? -1 : (v[0] == '1' ? 1 : 0);
+  }();
+  if (forced >= 0) return forced;
+  return mode == 1 ? 1 : 0;
+}
+
 bool want_pairs(const Shape& s) {
   (void)s;
   static const bool forced = [] {
@@ -662,6 +684,7 @@ cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void
   args.out = static_cast<__nv_bfloat16*>(h);
   args.ldo = s.F;
   args.status = status;
+  args.b_evict_first = b_evict_first(0);
   const int64_t max_tiles = max_m_tiles(s) * args.n_tiles;
   if (want_pairs(s)) {
     cudaError_t e = launch_pair<0>(a, a2, b, b2, args, max_tiles, st);
@@ -683,6 +706,7 @@ cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_dow
   args.out = static_cast<__nv_bfloat16*>(y);
   args.ldo = s.d;
   args.status = status;
+  args.b_evict_first = b_evict_first(1);
   if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
   if (s.d % 256 == 0) {
     args.n_tiles = s.d / 256;

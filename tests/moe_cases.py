@@ -8,7 +8,7 @@ Comparison rules (GPU vs the fp64 oracle on the same seeded inputs):
     oracle's grouping of the GPU's ids;
   * layer / MLP outputs: max-abs error <= 1e-2 * max|ref| (bf16 layers, float32
     accumulation) or <= 1e-4 * max|ref| (float32 layers);
-  * scores and gates: see score_tolerance().
+  * scores and gates: per token, see router_tolerance().
 """
 from __future__ import annotations
 
@@ -34,16 +34,35 @@ def out_tolerance(w: synth.Workload) -> float:
     return 1e-2 if w.dtype == "bf16" else 1e-4
 
 
-def score_tolerance(w: synth.Workload) -> float:
-    """Absolute tolerance of float32 scores and gates against the fp64 oracle.
+# Margin over the random-walk scale of float32 summation rounding (see router_tolerance).
+ROUND_MARGIN = 8.0
 
-    The logits are float32 sums of d exact products; their rounding error
-    behaves like a random walk of about 2^-24 * |partial sum| per term, i.e.
-    about 2^-24 * sqrt(d) * |l| overall. A renormalised gate moves by at most
-    2 * g * max|dl| <= 2 * max|dl|. With |l| <= 16 and a 4-sigma margin this
-    gives 1e-6 + 4 * 2 * 2^-24 * sqrt(d) * 16.
+
+def router_tolerance(x64: np.ndarray, wr64: np.ndarray, bias) -> np.ndarray:
+    """Per-token absolute tolerance [T] of float32 scores and gates against the fp64 oracle.
+
+    A logit is a float32 sum of the d products x_i * w_i (exact for bf16 inputs, each
+    rounded once for float32 inputs), plus the bias. Each rounding of a partial sum errs by
+    at most 2^-24 of it; the partial sums of d terms of random sign wander like a random
+    walk, so the accumulated error has the scale 2^-24 * sqrt(d) * ||x (.) w||_2 (the 2-norm
+    of the products, the random walk's step size times sqrt(d)), whatever order or grouping
+    (tensor-core k-blocks, split reductions) the sum takes. The tolerance of a logit is
+    ROUND_MARGIN times that scale for the token's largest such norm over the experts, plus
+    two roundings of the biased logit. A softmax or sigmoid score, and a renormalised gate,
+    moves by at most twice the largest logit error (d s_j = s_j (d l_j - sum_i s_i d l_i)
+    for softmax; gates g_j = s_j / sum s are s_j times a common factor), and the score
+    function's own float32 evaluation adds a few ulps of values at most 1: the 1e-6 floor.
     """
-    return 1e-6 + 8.0 * 2.0 ** -24 * math.sqrt(w.d_model) * 16.0
+    x64 = np.asarray(x64, dtype=np.float64)
+    wr64 = np.asarray(wr64, dtype=np.float64)
+    d = x64.shape[1]
+    p2 = np.sqrt((x64 * x64) @ (wr64 * wr64).T)               # [T, E] ||x_t (.) w_e||_2
+    l = x64 @ wr64.T
+    b = np.zeros(wr64.shape[0]) if bias is None else np.abs(np.asarray(bias, dtype=np.float64))
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float64)[None, :]
+    dl = 2.0 ** -24 * (ROUND_MARGIN * math.sqrt(d) * p2.max(axis=1) + 2.0 * (np.abs(l) + b[None, :]).max(axis=1))
+    return 1e-6 + 2.0 * dl
 
 
 class Inputs:

@@ -3,9 +3,10 @@
 Reduced workloads: every output element is compared. Full-size workloads (the
 five model-shaped layers, run exactly as the benchmark runs them, inputs
 generated on the device): routing and per-expert counts are compared for every
-token, and the layer output for a seeded sample of tokens that includes the
-first and last token, tokens of the busiest expert and (with capacity) fully
-or partly dropped tokens. The oracle regenerates the same inputs on the host.
+token; the layer output for every token of the decode batch and the tiny layer,
+and for the prefill layers a seeded sample of tokens that includes the first and
+last token, tokens of the busiest expert and (with capacity) fully or partly
+dropped tokens. The oracle regenerates the same inputs on the host.
 """
 import numpy as np
 import pytest
@@ -121,7 +122,9 @@ def test_layer_small_batches_repeat_on_one_workspace(name, edit):
 
 # ------------------------------------------------------------- full sizes
 
-def _sample_tokens(w, idx, dest_row, n=12):
+def _sample_tokens(w, idx, dest_row, n=32):
+    if w.T <= 64:                                   # the decode batch and the tiny layer: every token
+        return np.arange(w.T, dtype=np.int64)
     rng = np.random.default_rng(1234)
     toks = {0, w.T - 1}
     toks |= set(rng.choice(w.T, size=min(n, w.T), replace=False).tolist())

@@ -350,11 +350,6 @@ def test_memory_and_flops_table_from_page():
         assert O.flops_per_token(float(active)) / 1e9 == pytest.approx(float(gflop), rel=float(tol)), name
 
 
-def test_flops_per_pair_counts_three_matrices():
-    # one token through one SwiGLU expert: 3 matrices of d x F, 2 flops per multiply-add
-    assert O.flops_per_pair(4096, 14336) == 2 * 3 * 4096 * 14336
-
-
 # ------------------------------------------------------------- telemetry ---
 
 def test_routing_stats_hand_case():

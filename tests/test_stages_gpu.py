@@ -12,7 +12,7 @@ import torch
 import oracle as O
 import synth
 import sparse_expert_mlp_router_b300 as moe
-from moe_cases import Inputs, assert_close, cfg_of, check_routing, out_tolerance, score_tolerance, to_f64
+from moe_cases import Inputs, assert_close, cfg_of, check_routing, out_tolerance, router_tolerance, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -46,19 +46,34 @@ def test_router_shapes(edit):
     _check_router(synth.WORKLOADS["mini_qwen3"].with_(**edit))
 
 
-def _check_router(w):
-    inp = Inputs(w)
-    dev = inp.device()
+def _check_router(w, x64=None, wr64=None, bias=None, dev=None):
+    if dev is None:
+        inp = Inputs(w)
+        dev = inp.device()
+        x64, wr64, bias = inp.f64["x"], inp.f64["w_router"], inp.bias
     cfg = cfg_of(w)
-    idx, gate, scores, _, _ = _router(w, inp, dev, cfg)
-    ref_scores = O.scores_from_logits(O.router_logits(inp.f64["x"], inp.f64["w_router"], inp.bias), w.score)
-    tol = score_tolerance(w)
-    assert np.abs(scores - ref_scores).max() <= tol
+    idx, gate, scores, _, _ = _router(w, None, dev, cfg)
+    ref_scores = O.scores_from_logits(O.router_logits(x64, wr64, bias), w.score)
+    tol = router_tolerance(x64, wr64, bias)[:, None]          # [T, 1]: per token
+    err = np.abs(scores - ref_scores)
+    assert (err <= tol).all(), f"score error {float((err / tol).max()):.2f} x the token's tolerance"
     check_routing(idx, ref_scores, w.top_k)
     ref_gate = O.gates_from_scores(np.take_along_axis(ref_scores, idx.astype(np.int64), axis=1), w.renormalize)
-    assert np.abs(gate - ref_gate).max() <= tol
+    gerr = np.abs(gate - ref_gate)
+    assert (gerr <= tol).all(), f"gate error {float((gerr / tol).max()):.2f} x the token's tolerance"
     if w.renormalize:
         assert np.abs(gate.sum(axis=1) - 1.0).max() <= 1e-5
+
+
+@pytest.mark.parametrize("name", synth.workloads.FULL)
+def test_router_full_size(name):
+    # the five model-shaped routers on their full batches: scores and gates of every token
+    w = synth.WORKLOADS[name]
+    raw = {n: synth.host_tensor(w, n) for n in ("x", "w_router")}
+    bias = synth.router_bias(w.n_experts, w.bias_s)
+    dev = {n: synth.host_to_torch(a, w.dtype).cuda() for n, a in raw.items()}
+    dev["bias"] = None if bias is None else torch.from_numpy(bias).cuda()
+    _check_router(w, synth.as_f64(raw["x"], w.dtype), synth.as_f64(raw["w_router"], w.dtype), bias, dev)
 
 
 @pytest.mark.parametrize("name", MINI)
