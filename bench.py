@@ -64,10 +64,12 @@ HEADLINE = "mixtral_8x7b"
 EXTRA_WORKLOADS = ("qwen3_30b_a3b", "deepseek_v3", "decode_qwen3", "tiny_f32")
 # tokens whose expert MLPs the CPU oracle runs (the routing and grouping always cover the whole
 # batch); sized for a few seconds of fp64 work each, weights generated outside the timing
-CPU_SAMPLE_TOKENS = {"mixtral_8x7b": 2048, "qwen3_30b_a3b": 512, "deepseek_v3": 16, "decode_qwen3": 32,
+CPU_SAMPLE_TOKENS = {"mixtral_8x7b": 512, "qwen3_30b_a3b": 512, "deepseek_v3": 16, "decode_qwen3": 32,
                      "tiny_f32": 64}
-REF_TOKENS_PER_STEP = {"mixtral_8x7b": 64, "qwen3_30b_a3b": 64, "deepseek_v3": 2, "decode_qwen3": 32,
+REF_TOKENS_PER_STEP = {"mixtral_8x7b": 512, "qwen3_30b_a3b": 64, "deepseek_v3": 2, "decode_qwen3": 32,
                        "tiny_f32": 64}
+CPU_MIN_S = 0.5                      # CPU baseline: repeat a small sample to at least this much time
+CPU_MAX_REPS = 200
 # float32 FMA rate of the CUDA cores: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
 F32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
@@ -93,6 +95,9 @@ def parse_args(argv=None):
     ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
                     help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
                          "write_traffic) and exit")
+    ap.add_argument("--combine", choices=["separate", "fused"], default="separate",
+                    help="combine as its own kernel (default), or fused into the down projection's "
+                         "epilogue as float32 reductions (sets MOE_FUSED_COMBINE=1)")
     ap.add_argument("--eager", action="store_true",
                     help="time K separate launches of the layer instead of CUDA-graph replays")
     return ap.parse_args(argv)
@@ -387,20 +392,33 @@ class OracleSample:
                 f"weight generation excluded")
 
 
+ONE_CORE_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                "BLIS_NUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
 def cpu_baseline(w, n_tokens: int, one_core: bool = False) -> dict:
-    """The oracle timed once on a bounded sample of workload w (all host cores, or one)."""
+    """The oracle timed once on a bounded sample of workload w, on all host cores, or (one_core)
+    in a child process whose BLAS and OpenMP thread pools are limited to one thread."""
+    if one_core:
+        code = ("import json, sys; sys.path.insert(0, %r); import bench, synth; "
+                "print(json.dumps(bench.cpu_baseline(synth.WORKLOADS[%r], %d)))" % (ROOT, w.name, n_tokens))
+        r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **ONE_CORE_ENV), capture_output=True,
+                           text=True, timeout=600)
+        if r.returncode != 0:
+            return {"value": None, "error": r.stderr.strip().splitlines()[-1:] or ["failed"]}
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+        res["cores"] = 1
+        res["threads"] = "BLAS / OpenMP pools limited to 1 thread (" + ", ".join(sorted(ONE_CORE_ENV)) + ")"
+        return res
     s = OracleSample(w, n_tokens)
     toks = s.draw()
     s.preload([toks])
-    if one_core:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
-            n, dt = s.run(toks)
-        cores = 1
-    else:
-        n, dt = s.run(toks)
-        cores = cpu_threads()
-    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": s.describe(),
+    n, dt, reps = 0, 0.0, 0
+    while reps < CPU_MAX_REPS and (reps == 0 or dt < CPU_MIN_S):   # small layers: repeat to a measurable time
+        a, b = s.run(toks)
+        n, dt, reps = n + a, dt + b, reps + 1
+    return {"value": n / dt, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": s.describe() + (f", {reps} repetitions" if reps > 1 else ""),
             "seconds": dt, "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
@@ -725,6 +743,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
 
 def run_ours(args, w):
     import torch
+    if args.combine == "fused":
+        os.environ["MOE_FUSED_COMBINE"] = "1"
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     dist = None
@@ -741,7 +761,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": head["config"], "launch": "eager" if args.eager else "cuda_graph",
+        "config": head["config"], "launch": "eager" if args.eager else "cuda_graph", "combine": args.combine,
         "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "roofline": head["roofline"],
         "cpu_baseline": head["cpu_baseline"], "clocks": head["clocks"], "stages_ms": head["stages_ms"],
         "stages_sum_ms": head["stages_sum_ms"], "grouped_gemm_tflops": head["grouped_gemm_tflops"],

@@ -120,7 +120,29 @@ __global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
   }
 }
 
+// out = bf16(acc), eight elements (32 bytes in, 16 out) per thread step.
+__global__ void combine_finalize_kernel(const float4* __restrict__ acc, uint4* __restrict__ out, int64_t n8) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(a.x, a.y), p1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 p2 = __floats2bfloat162_rn(b.x, b.y), p3 = __floats2bfloat162_rn(b.z, b.w);
+    out[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
+                        *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_finalize(const Shape& s, const float* acc, void* out, cudaStream_t st) {
+  const int64_t n8 = (int64_t)s.T * s.d / 8;          // d is a multiple of 128 for bf16 layers
+  int64_t blocks = (n8 + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  combine_finalize_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
+                                                              static_cast<uint4*>(out), n8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_row, const float* gate, void* out,
                            int32_t* status, cudaStream_t st) {

@@ -84,51 +84,124 @@ struct GemmArgs {
   __nv_bfloat16* out;
   int64_t ldo;          // elements per output row
   int32_t* status;
-  int b_evict_first;    // load B (the weights) with an L2 evict-first policy
+  // MODE 2 (down projection with the combine in its epilogue) only:
+  const int32_t* src_token;   // [R] token of each routed row
+  const int32_t* dest_row;    // [T, k] grouped row of each (token, slot), -1 if dropped
+  const float* gate;          // [T, k] gates
+  float* acc_out;             // [T, d] float32 output accumulator, zeroed before the launch
+  int k;                      // slots per token
+  int routed_groups;          // E: groups >= E are the shared expert (weight one, row = token)
 };
 
-// Epilogue of one accumulator row (this thread's TMEM lane): output columns
-// [half * COLS/2, (half + 1) * COLS/2) of the tile, written at `orow`. MODE 0 reads gate
-// columns [0,128) and up columns [128,256) of the accumulator and writes COLS = 128.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+constexpr int kStageOutBytes = 32 * 64;   // one epilogue warp's staging: 32 rows x 32 bf16
+
+// Epilogue of one warp's 32 accumulator rows (TMEM lanes; this thread holds row `lane`):
+// output columns [half * COLS/2, (half + 1) * COLS/2) of the tile, rows 0 .. nvalid-1 written
+// at orow0 + r * ldo. MODE 0 reads gate columns [0,128) and up columns [128,256) of the
+// accumulator and writes COLS = 128 columns of silu(gate) * up.
+// Each 32-column chunk is converted to bf16 in registers (one 64-byte row piece per thread),
+// staged in the warp's 2 KB of shared memory, and read back so that each store instruction
+// writes 8 rows x 64 contiguous bytes (whole 32-byte sectors) instead of 32 rows x 16 bytes.
+// In the staging buffer, row r's 16-byte piece j sits at r * 64 + 16 * (j ^ ((r >> 1) & 3)),
+// which keeps both the row-wise writes and the column-wise reads free of bank conflicts.
 template <int MODE, int COLS>
-__device__ __forceinline__ void store_tile(uint32_t t_row, bool valid, __nv_bfloat16* orow, int half) {
+__device__ __forceinline__ void store_tile(uint32_t t_row, int nvalid, __nv_bfloat16* orow0, int64_t ldo, int half,
+                                           uint32_t stg, int lane) {
+  if (nvalid <= 0) return;                      // warp-uniform: no row of this warp is valid
   const int c0 = half * (COLS / 2), c1 = c0 + COLS / 2;
-  if (MODE == 0) {
 #pragma unroll 1
-    for (int c = c0; c < c1; c += 32) {
+  for (int c = c0; c < c1; c += 32) {
+    uint32_t packed[16];
+    if (MODE == 0) {
       uint32_t gv[32], uv[32];
       ptx::tmem_ld32(t_row + c, gv);
       ptx::tmem_ld32(t_row + 128 + c, uv);
       ptx::tmem_ld_wait();
-      if (valid) {
-        uint32_t packed[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
-          const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
-          packed[q] = pack_bf16(h0, h1);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      for (int q = 0; q < 16; ++q) {
+        const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
+        const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
+        packed[q] = pack_bf16(h0, h1);
       }
-    }
-  } else {
-#pragma unroll 1
-    for (int c = c0; c < c1; c += 32) {
+    } else {
       uint32_t v[32];
       ptx::tmem_ld32(t_row + c, v);
       ptx::tmem_ld_wait();
-      if (valid) {
-        uint32_t packed[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) packed[q] = pack_bf16(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+      for (int q = 0; q < 16; ++q) packed[q] = pack_bf16(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+    }
+    const uint32_t my_row = stg + (uint32_t)lane * 64u;
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(my_row + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+    __syncwarp();
+    const int j = lane & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = 8 * q + (lane >> 2);
+      const uint4 v = ld_shared_v4(stg + (uint32_t)r * 64u + ((uint32_t)(j ^ ((r >> 1) & 3)) << 4));
+      if (r < nvalid) *reinterpret_cast<uint4*>(orow0 + (int64_t)r * ldo + c + 8 * j) = v;
+    }
+    __syncwarp();
+  }
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Epilogue of MODE 2: the warp's 32 accumulator rows (this thread holds row `lane`; each row
+// is one (token, slot) pair, or one token of the shared expert) times their gates, added into
+// the tokens' float32 output rows. `arow` is this thread's row pointer (already offset to the
+// tile's first column), `ok` whether its row is added at all. Columns [half * COLS/2, ...).
+// As in store_tile, each 16-column piece goes through the warp's 2 KB staging buffer so that
+// one reduction instruction covers 8 rows x 64 contiguous bytes (whole sectors) instead of
+// 32 rows x 16 bytes; the row pointers and flags of other lanes come by shuffle.
+template <int COLS>
+__device__ __forceinline__ void combine_tile(uint32_t t_row, bool ok, float* arow, float gw, int half, uint32_t stg,
+                                             int lane) {
+  if (!__any_sync(0xffffffffu, ok)) return;
+  const int c0 = half * (COLS / 2), c1 = c0 + COLS / 2;
+  const uint32_t my_row = stg + (uint32_t)lane * 64u;
+  const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+  const int j = lane & 3;
+#pragma unroll 1
+  for (int c = c0; c < c1; c += 32) {
+    uint32_t v[32];
+    ptx::tmem_ld32(t_row + c, v);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        st_shared_v4(my_row + ((p ^ sw) << 4), __float_as_uint(gw * __uint_as_float(v[16 * hh + 4 * p])),
+                     __float_as_uint(gw * __uint_as_float(v[16 * hh + 4 * p + 1])),
+                     __float_as_uint(gw * __uint_as_float(v[16 * hh + 4 * p + 2])),
+                     __float_as_uint(gw * __uint_as_float(v[16 * hh + 4 * p + 3])));
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = 8 * q + (lane >> 2);
+        const uint4 u = ld_shared_v4(stg + (uint32_t)r * 64u + ((uint32_t)(j ^ ((r >> 1) & 3)) << 4));
+        float* dst = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(arow), r));
+        const bool rok = __shfl_sync(0xffffffffu, ok ? 1 : 0, r) != 0;
+        if (rok)
+          red_add_v4(dst + c + 16 * hh + 4 * j, __uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                     __uint_as_float(u.w));
       }
+      __syncwarp();
     }
   }
 }
@@ -145,8 +218,8 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (kStageBytes <= 32768) ? 6 : 4;
   static constexpr int kTmemCols = 2 * kNmma;                      // two accumulators
-  static constexpr size_t kSmem = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256 /*barriers*/ +
-                                  (size_t)kSchedInts * 4;
+  static constexpr size_t kStgOff = (size_t)kStages * kStageBytes + 256 + (((size_t)kSchedInts * 4 + 127) / 128) * 128;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStgOff + (size_t)kEpiWarps * kStageOutBytes;
 };
 
 template <int MODE, int BN>
@@ -171,6 +244,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   int32_t* s_a_row = s_tile_start + (args.G + 1);
   int32_t* s_out_row = s_a_row + args.G;
   int32_t* s_rows = s_out_row + args.G;
+  const uint32_t stg_base = ptx::smem_u32(smem + C::kStgOff);   // epilogue staging, 2 KB per warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,7 +291,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0;
       int issued = 0;              // loads issued (saturating at kStages)
       bool ok = true;
-      const uint64_t b_policy = ptx::l2_policy_evict_first();
       for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x) {
         int g, m, n;
         decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
@@ -234,13 +307,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t sb = sa + C::kABytes;
           ptx::mbar_arrive_expect_tx(fb, C::kStageBytes);
           ptx::tma_load_2d(sa, use_a2 ? (const void*)&tmA2 : (const void*)&tmA, kb * kBK, a_row, fb);
-          if (args.b_evict_first) {
-            ptx::tma_load_2d_hint(sb, &tmB, kb * kBK, b_row, fb, b_policy);
-            if (MODE == 0) ptx::tma_load_2d_hint(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb, b_policy);
-          } else {
-            ptx::tma_load_2d(sb, &tmB, kb * kBK, b_row, fb);
-            if (MODE == 0) ptx::tma_load_2d(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb);
-          }
+          ptx::tma_load_2d(sb, &tmB, kb * kBK, b_row, fb);
+          if (MODE == 0) ptx::tma_load_2d(sb + 128 * 128, &tmB2, kb * kBK, b_row, fb);
           if (issued < C::kStages) ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -322,9 +390,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       ptx::tc_fence_after();
       const bool valid = (m * kBM + r_local) < s_rows[g];
       const int64_t out_row = (int64_t)s_out_row[g] + m * kBM + r_local;
-      __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * C::kOutCols;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::kNmma);
-      store_tile<MODE, C::kOutCols>(t_row, valid, orow, half);
+      if constexpr (MODE == 2) {
+        // the pair's token and gate: the slot of the token whose dest_row names this row
+        int tok = 0;
+        float gw = 0.0f;
+        bool ok_row = valid;
+        if (valid) {
+          if (g >= args.routed_groups) {
+            tok = m * kBM + r_local;
+            gw = 1.0f;
+          } else {
+            tok = args.src_token[out_row];
+            ok_row = false;
+            for (int j = 0; j < args.k; ++j)
+              if (args.dest_row[(int64_t)tok * args.k + j] == (int32_t)out_row) {
+                gw = args.gate[(int64_t)tok * args.k + j];
+                ok_row = true;
+              }
+            if (!ok_row) set_status(args.status, MOE_ERR_DEVICE_INDEX);
+          }
+        }
+        combine_tile<C::kOutCols>(t_row, ok_row, args.acc_out + (int64_t)tok * args.ldo + (int64_t)n * C::kOutCols,
+                                  gw, half, stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
+      } else {
+        const int row0 = m * kBM + quarter * 32;                // the warp's first row in the group
+        __nv_bfloat16* orow0 = args.out + ((int64_t)s_out_row[g] + row0) * args.ldo + (int64_t)n * C::kOutCols;
+        store_tile<MODE, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
+                                      stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty[acc]));
     }
@@ -350,7 +444,8 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;            // 32 KB
   static constexpr int kStages = 6;
   static constexpr int kTmemCols = 2 * kN;                         // two accumulators (512)
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256 + (size_t)kSchedInts * 4;
+  static constexpr size_t kStgOff = (size_t)kStages * kStageBytes + 256 + (((size_t)kSchedInts * 4 + 127) / 128) * 128;
+  static constexpr size_t kSmem = 1024 + kStgOff + (size_t)kEpiWarps * kStageOutBytes;
 };
 
 template <int MODE>
@@ -376,6 +471,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   int32_t* s_out_row = s_a_row + args.G;
   int32_t* s_rows = s_out_row + args.G;
   int32_t* s_pair_start = s_rows + args.G;     // [G+1] prefix of 256-row tiles per group
+  const uint32_t stg_base = ptx::smem_u32(smem + C::kStgOff);   // epilogue staging, 2 KB per warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -535,7 +631,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int r_local = quarter * 32 + lane;
     const uint32_t tempty_leader = ptx::map_shared_rank(ptx::smem_u32(tempty), 0);
     int it = 0;
     for (int L = unit0; L < total_tiles; L += unit_step, ++it) {
@@ -550,11 +645,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         break;
       }
       ptx::tc_fence_after();
-      const bool valid = (m * kBM + r_local) < s_rows[g];
-      const int64_t out_row = (int64_t)s_out_row[g] + m * kBM + r_local;
-      __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * C::kOutCols;
+      const int row0 = m * kBM + quarter * 32;
+      __nv_bfloat16* orow0 = args.out + ((int64_t)s_out_row[g] + row0) * args.ldo + (int64_t)n * C::kOutCols;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::kN);
-      store_tile<MODE, C::kOutCols>(t_row, valid, orow, half);
+      store_tile<MODE, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
+                                    stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(tempty_leader + 8u * acc);
     }
@@ -590,21 +685,6 @@ bool pairs_fit(const cudaLaunchConfig_t& cfg) {
 // few percent of the single-CTA kernel on the tensor-bound layers (all of them run at the
 // power limit) and slower where experts have few rows (decode, capacity-limited layers),
 // where a 256-row tile doubles the wasted MMA work.
-// Whether the weights (B) of a grouped GEMM are loaded with the L2 evict-first policy. The
-// m-tiles that read one weight tile run in the same wave, so the weights need L2 only briefly,
-// while the activation rows (A) are read again by later waves for the other n-tiles: with
-// evict-first on the weights, L2 keeps the activations. Default: on for the down projection
-// (K = d_ff is long, so an expert's h rows are the larger reuse set), off for gate/up;
-// MOE_GEMM_B_EVICT_FIRST=0/1 (read once per process) sets both.
-int b_evict_first(int mode) {
-  static const int forced = [] {
-    const char* v = getenv("MOE_GEMM_B_EVICT_FIRST");
-    return v == nullptr ? -1 : (v[0] == '1' ? 1 : 0);
-  }();
-  if (forced >= 0) return forced;
-  return mode == 1 ? 1 : 0;
-}
-
 bool want_pairs(const Shape& s) {
   (void)s;
   static const bool forced = [] {
@@ -684,7 +764,6 @@ cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void
   args.out = static_cast<__nv_bfloat16*>(h);
   args.ldo = s.F;
   args.status = status;
-  args.b_evict_first = b_evict_first(0);
   const int64_t max_tiles = max_m_tiles(s) * args.n_tiles;
   if (want_pairs(s)) {
     cudaError_t e = launch_pair<0>(a, a2, b, b2, args, max_tiles, st);
@@ -706,7 +785,6 @@ cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_dow
   args.out = static_cast<__nv_bfloat16*>(y);
   args.ldo = s.d;
   args.status = status;
-  args.b_evict_first = b_evict_first(1);
   if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
   if (s.d % 256 == 0) {
     args.n_tiles = s.d / 256;
@@ -723,6 +801,37 @@ cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_dow
   args.n_tiles = s.d / 128;
   if (!make_tmap_bf16(&b, w_down, s.F, (uint64_t)s.G * s.d, 128)) return cudaErrorInvalidValue;
   return launch_single<1, 128>(a, a, b, b, args, max_m_tiles(s) * args.n_tiles, st);
+}
+
+cudaError_t launch_gemm_down_combine_tc(const Shape& s, const void* h, const void* w_down, const void* sched,
+                                        const int32_t* src_token, const int32_t* dest_row, const float* gate,
+                                        float* acc_out, int32_t* status, cudaStream_t st) {
+  CUtensorMap a, b;
+  const uint64_t rows = (uint64_t)s.R + (uint64_t)s.S * s.T;
+  GemmArgs args{};
+  args.K = s.F;
+  args.G = s.G;
+  args.shared_from = s.G;
+  args.b_rows = s.d;
+  args.sched = static_cast<const int32_t*>(sched);
+  args.out = nullptr;
+  args.ldo = s.d;
+  args.status = status;
+  args.src_token = src_token;
+  args.dest_row = dest_row;
+  args.gate = gate;
+  args.acc_out = acc_out;
+  args.k = s.k;
+  args.routed_groups = s.E;
+  if (!make_tmap_bf16(&a, h, s.F, rows > 0 ? rows : 1, kBM)) return cudaErrorInvalidValue;
+  if (s.d % 256 == 0) {
+    args.n_tiles = s.d / 256;
+    if (!make_tmap_bf16(&b, w_down, s.F, (uint64_t)s.G * s.d, 256)) return cudaErrorInvalidValue;
+    return launch_single<2, 256>(a, a, b, b, args, max_m_tiles(s) * args.n_tiles, st);
+  }
+  args.n_tiles = s.d / 128;
+  if (!make_tmap_bf16(&b, w_down, s.F, (uint64_t)s.G * s.d, 128)) return cudaErrorInvalidValue;
+  return launch_single<2, 128>(a, a, b, b, args, max_m_tiles(s) * args.n_tiles, st);
 }
 
 }  // namespace moe

@@ -29,7 +29,8 @@ struct WsLayout {
   size_t src_token;     // [R] int32
   size_t x_perm;        // [R*d] elements
   size_t h;             // [(R+S*T)*F] elements: silu(gate) * up
-  size_t y;             // [(R+S*T)*d] elements: expert outputs
+  size_t y;             // [(R+S*T)*d] elements: expert outputs; with the fused combine, the
+                        // [T*d] float32 output accumulator instead (the region holds either)
   size_t total;
 };
 
@@ -120,6 +121,13 @@ cudaError_t launch_gemm_gateup_tc(const Shape& s, const void* x_perm, const void
                                   int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_down_tc(const Shape& s, const void* h, const void* w_down,
                                 const void* sched, void* y, int32_t* status, cudaStream_t st);
+// The down projection with the combine in its epilogue: each row's output times its gate
+// (one for the shared expert) is added in float32 into acc_out [T, d] (zeroed beforehand).
+cudaError_t launch_gemm_down_combine_tc(const Shape& s, const void* h, const void* w_down, const void* sched,
+                                        const int32_t* src_token, const int32_t* dest_row, const float* gate,
+                                        float* acc_out, int32_t* status, cudaStream_t st);
+// out [T, d] bf16 = acc [T, d] float32, rounded once.
+cudaError_t launch_combine_finalize(const Shape& s, const float* acc, void* out, cudaStream_t st);
 
 // FP8 (E4M3) expert weights with per-row float32 scales (gemm_fp8w.cu).
 bool fp8w_supported(const Shape& s);

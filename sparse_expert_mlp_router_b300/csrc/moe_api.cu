@@ -3,6 +3,7 @@
 // include/moe.h.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include <nvtx3/nvToolsExt.h>
@@ -118,7 +119,9 @@ WsLayout make_layout(const Shape& s) {
   L.src_token = take((size_t)s.R * 4);
   L.x_perm = take((size_t)s.R * s.d * s.esize);
   L.h = take(grouped * s.F * s.esize);
-  L.y = take(grouped * s.d * s.esize);
+  size_t y_bytes = grouped * s.d * s.esize;
+  if (s.dtype == MOE_BF16 && y_bytes < (size_t)s.T * s.d * 4) y_bytes = (size_t)s.T * s.d * 4;   // fused combine
+  L.y = take(y_bytes);
   L.total = o;
   return L;
 }
@@ -229,6 +232,18 @@ moe_status_t check_fp8_weights(const Shape& s, const uint8_t* wg_q, const float*
   return MOE_OK;
 }
 
+// Whether the whole-layer call runs the down projection with the combine in its epilogue
+// (float32 reductions into an output accumulator, then one rounding pass) instead of writing
+// the grouped expert outputs and combining them in a separate kernel. bf16 layers with bf16
+// weights only; selected by MOE_FUSED_COMBINE=1 in the environment, read at every call. The
+// order of the float32 additions then depends on scheduling, so the output is not
+// bit-reproducible from run to run (the separate combine's is).
+bool fused_combine(const Shape& s, const ExpertWeights& w) {
+  if (s.dtype != MOE_BF16 || w.fp8) return false;
+  const char* v = getenv("MOE_FUSED_COMBINE");
+  return v != nullptr && v[0] == '1';
+}
+
 // Kernel launches one moe_layer_forward enqueues.
 int layer_launches(const Shape& s) {
   // hist, scan (+ group schedule), scatter, gather; one CTA for the first three when the batch
@@ -281,14 +296,28 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
       return MOE_ERR_CUDA;
   }
   if (!mark(2)) return MOE_ERR_CUDA;
+  const bool fused = fused_combine(s, w);
+  float* acc = at<float>(ws, L.y);
   {
     const NvtxRange r("moe_layer/experts");
-    if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) return MOE_ERR_CUDA;
+    if (fused) {
+      void* sched = at<void>(ws, L.sched);
+      void* h = at<void>(ws, L.h);
+      if (launch_gemm_gateup_tc(s, x_perm, x, w.g, w.u, sched, h, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+      if (!mark(3)) return MOE_ERR_CUDA;
+      if (cudaMemsetAsync(acc, 0, (size_t)s.T * s.d * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
+      if (launch_gemm_down_combine_tc(s, h, w.d, sched, src_token, dest_row, gate, acc, status, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) {
+      return MOE_ERR_CUDA;
+    }
   }
   if (!mark(4)) return MOE_ERR_CUDA;
   {
     const NvtxRange r("moe_layer/combine");
-    if (launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (fused ? launch_combine_finalize(s, acc, out, st) != cudaSuccess
+              : launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   if (!mark(5)) return MOE_ERR_CUDA;
   return MOE_OK;

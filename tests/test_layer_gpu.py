@@ -166,3 +166,42 @@ def test_layer_full_size_sampled(name):
     assert_close(got, res.out, out_tolerance(w), name)
     del dev
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------- fused down-projection + combine
+
+@pytest.mark.parametrize("name,edit", [
+    ("mini_mixtral", {}),
+    ("mini_qwen3", {}),
+    ("mini_deepseek", {}),                                         # drops, shared expert (weight one)
+    ("mini_decode", {}),
+    ("mini_deepseek", dict(capacity_factor=0.05)),                 # almost everything dropped
+    ("mini_mixtral", dict(T=1)),
+    ("mini_qwen3", dict(top_k=1)),                                 # accumulator larger than the grouped rows
+    ("mini_qwen3", dict(bias_s=8.0, top_k=2)),                     # mostly empty experts
+])
+def test_layer_fused_combine(name, edit, monkeypatch):
+    # the down projection adds gate * y into a float32 accumulator in its epilogue, then one
+    # rounding pass writes the output: same oracle comparison as the separate combine
+    monkeypatch.setenv("MOE_FUSED_COMBINE", "1")
+    w = synth.WORKLOADS[name].with_(**edit)
+    inp = Inputs(w)
+    out, idx, counts = _run_layer(w, inp.device(), cfg_of(w))
+    res, _ = _oracle_on_gpu_routing(w, inp.f64["x"], inp.f64["w_router"], inp.bias, inp.expert, idx)
+    assert (counts == res.disp.counts).all()
+    assert_close(to_f64(out), res.out, out_tolerance(w), f"fused {name} {edit}")
+
+
+def test_layer_fused_combine_full_size_qwen3(monkeypatch):
+    w = synth.WORKLOADS["qwen3_30b_a3b"]
+    cfg = cfg_of(w)
+    dev = synth.device_inputs(w)
+    ref_out, ref_idx, _ = _run_layer(w, dev, cfg)                  # the separate combine
+    monkeypatch.setenv("MOE_FUSED_COMBINE", "1")
+    out, idx, _ = _run_layer(w, dev, cfg)
+    assert (idx == ref_idx).all()
+    # both are within 1e-2 of the oracle; against each other they differ by the rounding of y
+    # to bf16 (separate path) and the order of the float32 additions
+    assert_close(to_f64(out), to_f64(ref_out), 1e-2, "fused vs separate combine")
+    del dev
+    torch.cuda.empty_cache()
