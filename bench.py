@@ -15,18 +15,17 @@ run and reported under "workloads", one entry each.
 value        tokens/s with inputs resident in HBM: K steps timed with CUDA events
              (barrier + synchronize on both sides, max over ranks); the expert
              weights exceed the 126 MB L2, so every step streams them from HBM.
-             The K moe_layer_forward calls run as CUDA-graph replays of plain layer
-             calls, in four chunks; after each timed chunk the same calls replay with
-             CUDA events at the stage boundaries (untimed for `value`), so the stage
-             times and the layer time are taken under the same clocks and power.
-             --eager: K separate calls with the stage events, timed as they run.
+             The K moe_layer_forward calls run as one CUDA-graph replay; about one
+             layer in 25 (at least four) carries CUDA events at the stage boundaries,
+             so the stage times come from the timed replay itself, under the same
+             clocks and power. --eager: K separate calls with the stage events.
 e2e          the same metric through the same C-ABI call with the activations in
              pinned host memory: each step copies x host->device, runs the layer and
              copies out device->host. Steps with at least 1 MB of activations run their
              copies on their own streams, overlapping the neighbouring steps' layers;
              smaller steps run serially on one stream. Both loops are reported.
 roofline     the dominant kernel (the gate/up grouped GEMM), timed by events recorded
-             around it on the launching stream, in the staged replays.
+             around it on the launching stream, in the layers that carry them.
 cpu_baseline the fp64 CPU oracle on a bounded sample of the same workload: the whole
              batch's routing and grouping, the expert MLPs and combine of a token sample.
 --impl reference  times that oracle alone on the host cores, step by step, each step
@@ -56,7 +55,6 @@ UNIT = "tokens/s"
 OVERLAP_MIN_BYTES = 1 << 20          # end-to-end loop: overlap the copies from this size
 E2E_WARM_S = 0.3                     # end-to-end loops: warm-up wall time
 E2E_MIN_S = 0.3                      # end-to-end loops: least timed device time
-TIMED_CHUNKS = 4                     # plain / staged replay pairs the K timed steps are split into
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -475,11 +473,11 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------- our layer
 
-def chunk_sizes(K: int, n: int = TIMED_CHUNKS) -> list:
-    """K steps split into at most n chunks of at most two sizes (largest first)."""
-    n = max(1, min(n, K))
-    base, extra = divmod(K, n)
-    return [base + 1] * extra + [base] * (n - extra)
+def staged_positions(K: int) -> list:
+    """Which of the K timed layers carry the stage events: about one in 25 (at least
+    min(K, 4) of them), evenly spread, the last one included."""
+    n = min(K, max(4, K // 25))
+    return [((j + 1) * K) // n - 1 for j in range(n)]
 
 
 def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
@@ -531,33 +529,30 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     work = algorithmic(w, kept, touched, 1.0 if fp8 else (2.0 if w.dtype == "bf16" else 4.0))
 
     K, W = args.steps, args.warmup
-    sizes = chunk_sizes(K) if not args.eager else [K]
-    n_ev = max(sizes)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_ev)]
+    # Graph mode: the K timed steps are one CUDA-graph replay of K layer calls; a few of them,
+    # evenly spread (staged_positions), are recorded with CUDA events at the five stage
+    # boundaries, so the stage times come from the timed replay itself (six event records cost
+    # a decode-shaped layer about 8 %, and only these layers carry them). Eager mode (--eager,
+    # for profilers): K separate calls, each with the stage events.
+    staged_at = staged_positions(K) if not args.eager else list(range(K))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(len(staged_at))]
     for row in evs:            # create every event before any capture
         for e in row:
             e.record()
     for i in range(W):
-        forward_timed(*args_fwd, evs[i % n_ev])
+        forward_timed(*args_fwd, evs[i % len(evs)])
     barrier()
-    # Graph mode: the K timed steps are CUDA-graph replays of plain moe_layer_forward calls in
-    # TIMED_CHUNKS chunks; after each timed chunk the same number of calls replays with CUDA
-    # events at the five stage boundaries (six event records a layer cost the decode-shaped
-    # layer about 8 %, so they stay out of the timed replays). Alternating the two keeps the
-    # stage times under the same clocks and power as the timed layers.
-    plain, staged = {}, {}
+    graph = None
     if not args.eager:
-        for n in sorted(set(sizes)):
-            plain[n] = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(plain[n]):
-                for i in range(n):
+        slot = {pos: j for j, pos in enumerate(staged_at)}
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(K):
+                if i in slot:
+                    forward_timed(*args_fwd, evs[slot[i]])
+                else:
                     forward(*args_fwd)
-            staged[n] = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(staged[n]):
-                for i in range(n):
-                    forward_timed(*args_fwd, evs[i])
-            plain[n].replay()      # one untimed replay of each
-            staged[n].replay()
+        graph.replay()             # one untimed replay
         barrier()
     props = torch.cuda.get_device_properties(local)
     try:
@@ -568,31 +563,24 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     sampler.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    elapsed_ms = 0.0
-    stage_rows = []
-    for n in sizes:
-        barrier()
-        t_start.record()
-        if args.eager:
-            for i in range(n):
-                forward_timed(*args_fwd, evs[i])
-        else:
-            plain[n].replay()
-        t_end.record()
-        barrier()
-        elapsed_ms += t_start.elapsed_time(t_end)
-        if not args.eager:
-            staged[n].replay()
-            torch.cuda.synchronize()
-        stage_rows += [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(n)]
+    barrier()
+    t_start.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(K):
+            forward_timed(*args_fwd, evs[i])
+    t_end.record()
+    barrier()
     clocks = sampler.stop()
-    stage = np.array(stage_rows)       # [K, 5] ms
+    elapsed_ms = t_start.elapsed_time(t_end)
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in evs])   # [staged layers, 5] ms
     status = moe.moe_get_device_error(ws)
     if status != moe.MOE_OK:
         raise RuntimeError(f"{w.name}: device status after timing: {moe.status_string(status)}")
     max_ms = max_over_ranks(elapsed_ms, dist)
     value = whole_job_rate(w.T, K, world, max_ms)
-    del plain, staged
+    del graph
 
     # end to end: activations in pinned host memory, copies inside the timed region. Two loops:
     # serial (one stream: copy x in, run the layer, copy the output out), and overlapped (the

@@ -101,3 +101,12 @@ def test_source_hash_ignores_comments_but_not_code():
     assert bench.code_only(src) == bench.code_only(recommented)
     assert bench.code_only(src) != bench.code_only(changed)
     assert len(bench.kernel_source_hash("bf16")) == 64
+
+
+def test_stage_event_layers_are_spread_over_the_timed_replay():
+    for K in (1, 3, 4, 20, 100, 500, 1001):
+        pos = bench.staged_positions(K)
+        assert len(pos) == min(K, max(4, K // 25))
+        assert pos == sorted(set(pos)) and pos[-1] == K - 1 and pos[0] >= 0
+        gaps = [b - a for a, b in zip([-1] + pos, pos)]
+        assert max(gaps) - min(gaps) <= 1                 # evenly spread
