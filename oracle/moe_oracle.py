@@ -35,6 +35,8 @@ What the layer computes (the plainest reading of the pages):
      expert's MLP of x[t] with weight one           [ST "The router" (shared experts); KG definition]
 The residual add is outside the layer: a token whose every routed pair was
 dropped gets only its shared-expert part (zero when there is none).
+With FP8 (E4M3) weights the expert MLP runs on the dequantized weights; with FP8
+activations as well (W8A8, a mode beyond the pages) it is expert_mlp_w8a8.
 
 Readings where the pages are silent (each the plainest one):
   * tie-break of equal scores: the lower expert index wins; slot order is the
@@ -65,6 +67,7 @@ __all__ = [
     "capacity", "dispatch", "silu", "expert_mlp", "combine", "layer_forward", "LayerResult",
     "flops_per_token", "weight_bytes", "experts_touched_expected", "experts_touched",
     "routing_stats", "e4m3_decode", "e4m3_encode", "quantize_fp8_rows", "dequantize_fp8_rows",
+    "bf16_round", "expert_mlp_w8a8",
 ]
 
 
@@ -231,7 +234,8 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
                   *, top_k: int, score: str = "softmax", renormalize: bool = True,
                   capacity_factor: float = 0.0, n_shared: int = 0,
                   tokens: Optional[np.ndarray] = None,
-                  routing: Optional[tuple] = None) -> LayerResult:
+                  routing: Optional[tuple] = None,
+                  mlp: Callable = None) -> LayerResult:
     """The MoE FFN layer for all tokens, or only the outputs of `tokens`.
 
     x [T,d] and w_router [E,d] are float64 (exact copies of the stored
@@ -240,7 +244,9 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
     and capacity always cover all T tokens (admission depends on the whole
     batch); only the MLP and combine are restricted to `tokens`.
     `routing` = (idx, gate) replaces stages 1-4 (scores then come back None).
+    `mlp` replaces the expert MLP (expert_mlp_w8a8 for FP8 activations).
     """
+    mlp = expert_mlp if mlp is None else mlp
     x = np.asarray(x, dtype=np.float64)
     T, d = x.shape
     E = w_router.shape[0]
@@ -264,14 +270,14 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
         if rows.size == 0:
             continue
         wg, wu, wd = experts(e)
-        y_rows[rows] = expert_mlp(x[disp.src_token[rows]], wg, wu, wd)
+        y_rows[rows] = mlp(x[disp.src_token[rows]], wg, wu, wd)
 
     shared = None
     if n_shared > 0:
         shared = np.zeros((T, d), dtype=np.float64)
         for s_i in range(n_shared):
             wg, wu, wd = experts(E + s_i)
-            shared[tok] += expert_mlp(x[tok], wg, wu, wd)
+            shared[tok] += mlp(x[tok], wg, wu, wd)
     out = combine(disp.dest_row, gate, y_rows, shared, d)[tok]
     return LayerResult(idx, gate, s, disp, cap, tok, out)
 
@@ -384,3 +390,37 @@ def quantize_fp8_rows(w) -> tuple:
 def dequantize_fp8_rows(codes, scale) -> np.ndarray:
     """scale[r] * value(code[r][c]) in float64 (exact)."""
     return np.asarray(scale, dtype=np.float64)[..., None] * e4m3_decode(codes)
+
+
+# ---------------------------------------------------------------------------
+# FP8 activations as well (W8A8)
+#
+# A reading beyond what the pages fix. The pages put the weights in FP8 (the 671B model in
+# ~671 GB) and say nothing of the activations; this mode also stores the activations that
+# enter each expert contraction in E4M3, quantised per row exactly as the weights are (one
+# float32 scale per row, scale = max|row| / 448, code = E4M3 of value / scale): the expert's
+# input rows before the gate/up products, and the intermediate h = silu(g) * u -- which is
+# stored in bf16 between the two contractions -- before the down product. Products and sums
+# are then exact in the quantised values. It changes the layer's numbers by the activations'
+# quantisation error (about 2^-4 of an element at most), so it is compared with this
+# function, not with the bf16-activation layer.
+
+def bf16_round(v) -> np.ndarray:
+    """Values rounded to float32, then to bfloat16 with round-to-nearest-even (float64 out):
+    how a float32 result is stored in bf16."""
+    u = np.ascontiguousarray(np.asarray(v, dtype=np.float64).astype(np.float32)).view(np.uint32).astype(np.uint64)
+    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return (u.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def expert_mlp_w8a8(xrows: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray) -> np.ndarray:
+    """The SwiGLU expert MLP with E4M3 activations: x rows quantised per row, gate and up
+    products of the quantised rows, h = silu(g) * u stored in bf16 and quantised per row,
+    down product of the quantised h. Same shapes as expert_mlp."""
+    qx, sx = quantize_fp8_rows(np.asarray(xrows, dtype=np.float64))
+    xq = dequantize_fp8_rows(qx, sx)
+    g = xq @ np.asarray(w_gate, dtype=np.float64).T
+    u = xq @ np.asarray(w_up, dtype=np.float64).T
+    h = bf16_round(silu(g) * u)
+    qh, sh = quantize_fp8_rows(h)
+    return dequantize_fp8_rows(qh, sh) @ np.asarray(w_down, dtype=np.float64).T

@@ -16,6 +16,8 @@ import numpy as np
 import pytest
 
 import oracle as O
+import synth
+import torch
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -416,3 +418,66 @@ def test_quantize_rows_error_bound_and_scale():
     err = np.abs(deq[rows] - w[rows].astype(np.float64))
     bound = np.maximum(np.abs(w[rows]) * 2.0 ** -4, s[rows, None] * 2.0 ** -10) * (1 + 1e-6)
     assert (err <= bound).all()
+
+
+# --------------------------------------------------------- FP8 activations ---
+
+def test_bf16_round_matches_the_format():
+    # hand values: exact ones stay, a tie rounds to the even mantissa, just above a tie rounds up
+    one = 1.0
+    assert O.bf16_round([one, -2.5, 0.0])[0] == 1.0
+    assert O.bf16_round([1.0 + 2.0 ** -8])[0] == 1.0                       # tie -> even (1.0)
+    assert O.bf16_round([1.0 + 3 * 2.0 ** -8])[0] == 1.0 + 2.0 ** -6       # tie -> even (1 + 2^-6)
+    assert O.bf16_round([1.0 + 2.0 ** -8 + 2.0 ** -20])[0] == 1.0 + 2.0 ** -7
+    # and torch's float32 -> bfloat16 conversion (round to nearest even) on random values
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(4096) * np.exp(rng.uniform(-20, 20, 4096))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy().astype(np.float64)
+    assert np.array_equal(O.bf16_round(v), ref)
+
+
+def test_w8a8_mlp_one_element_closed_form():
+    # d = F = 1: a one-element row quantises to +-448 times its scale, i.e. to itself up to the
+    # float32 rounding of the scale, so the W8A8 MLP is c * bf16(silu(a x) * b x)
+    for x0, a, b, c in [(0.75, 1.5, -2.0, 0.5), (-3.0, 0.25, 0.125, -1.0), (1e-3, 40.0, 2.0, 3.0)]:
+        y = O.expert_mlp_w8a8(np.array([[x0]]), np.array([[a]]), np.array([[b]]), np.array([[c]]))[0, 0]
+        z = a * x0
+        h = O.bf16_round([z / (1.0 + math.exp(-z)) * (b * x0)])[0]
+        assert y == pytest.approx(c * h, rel=1e-6)
+
+
+def test_w8a8_mlp_error_is_the_activation_quantisation_error():
+    # random bf16-like rows through a 256 -> 128 -> 256 expert: the W8A8 output differs from the
+    # exact MLP by E4M3's relative precision (3 mantissa bits: at most 2^-4 of an element,
+    # about 2^-4 / sqrt(3) in rms), so the relative max error sits between 0.1 % and 8 %:
+    # no quantisation (error 0) or a dropped or doubled scale (error ~100 %) fall outside
+    rng = np.random.default_rng(11)
+    d, F = 256, 128
+    x = O.bf16_round(rng.standard_normal((64, d)))
+    wg, wu = (O.bf16_round(rng.standard_normal((F, d)) * 0.05) for _ in range(2))
+    wd = O.bf16_round(rng.standard_normal((d, F)) * 0.05)
+    exact = O.expert_mlp(x, wg, wu, wd)
+    got = O.expert_mlp_w8a8(x, wg, wu, wd)
+    rel = np.abs(got - exact).max() / np.abs(exact).max()
+    assert 1e-3 < rel < 8e-2, rel
+    # scaling an input row by a power of two changes only its scale, by the same power of two:
+    # the quantised rows scale exactly
+    q1, s1 = O.quantize_fp8_rows(x)
+    q2, s2 = O.quantize_fp8_rows(x * 8.0)
+    assert np.array_equal(q1, q2) and np.array_equal(s2, s1 * np.float32(8.0))
+
+
+def test_layer_forward_takes_the_w8a8_mlp():
+    # the layer with the W8A8 MLP equals the same routing and combine over expert_mlp_w8a8
+    w = synth.WORKLOADS["mini_qwen3"].with_(T=40, n_experts=8, top_k=2, d_model=128, d_ff=128)
+    x = synth.as_f64(synth.host_tensor(w, "x"), w.dtype)
+    wr = synth.as_f64(synth.host_tensor(w, "w_router"), w.dtype)
+    ex = {g: tuple(synth.as_f64(a, w.dtype) for a in synth.host_expert(w, g)) for g in range(w.n_experts)}
+    res = O.layer_forward(x, wr, None, ex.__getitem__, top_k=2, mlp=O.expert_mlp_w8a8)
+    plain = O.layer_forward(x, wr, None, ex.__getitem__, top_k=2)
+    assert (res.idx == plain.idx).all()
+    for t in (0, 17, 39):
+        want = sum(res.gate[t, j] * O.expert_mlp_w8a8(x[t:t + 1], *ex[int(res.idx[t, j])])[0] for j in range(2))
+        assert np.allclose(res.out[t], want, rtol=0, atol=1e-12)
+    rel = np.abs(res.out - plain.out).max() / np.abs(plain.out).max()
+    assert 1e-4 < rel < 8e-2
