@@ -88,8 +88,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=None,
                     help="tokens whose expert MLPs the CPU oracle runs (default: per workload)")
-    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
-                    help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales")
+    ap.add_argument("--weights", choices=["bf16", "fp8", "w8a8"], default="bf16",
+                    help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales (fp8), or "
+                         "those weights with the expert inputs quantised to E4M3 per row as well (w8a8)")
     ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
                     help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
                          "write_traffic) and exit")
@@ -207,7 +208,8 @@ class ClockSampler:
 
 
 GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh"),
-                "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh")}
+                "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh"),
+                "w8a8": ("gemm_w8a8.cu", "fp8_quant.cuh", "gemm_common.cuh", "tc_ptx.cuh")}
 
 
 def code_only(src: str) -> str:
@@ -302,7 +304,7 @@ def cpu_model() -> str:
 
 def config_of(w, kept: int, touched: int, world: int, weights: str) -> dict:
     """The `config` object of a bench line: what the workload is, identical in both arms."""
-    fp8 = weights == "fp8"
+    fp8 = weights in ("fp8", "w8a8")
     return {"workload": w.name, "T": w.T, "d_model": w.d_model, "n_experts": w.n_experts,
             "n_shared": w.n_shared, "top_k": w.top_k, "d_ff": w.d_ff, "score": w.score,
             "renormalize": bool(w.renormalize), "capacity_factor": w.capacity_factor, "kept_pairs": int(kept),
@@ -313,7 +315,8 @@ def config_of(w, kept: int, touched: int, world: int, weights: str) -> dict:
                   "inputs smaller than L2 (%.1f MB of expert weights): a latency-bound layer"
                   % (touched * 3.0 * w.d_model * w.d_ff * (2 if w.dtype == "bf16" else 4) / 1e6),
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "weights": "fp8 e4m3, per-row float32 scales" if fp8 else w.dtype}
+            "weights": ("fp8 e4m3, per-row float32 scales" + (
+                "; activations e4m3 per row too (w8a8)" if weights == "w8a8" else "")) if fp8 else w.dtype}
 
 
 # ----------------------------------------------------------- the CPU oracle
@@ -497,7 +500,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
                           n_shared=w.n_shared, score=w.score, renormalize=w.renormalize,
                           capacity_factor=w.capacity_factor, dtype=w.dtype)
     dev = synth.device_inputs(w)
-    fp8 = args.weights == "fp8" and w.dtype == "bf16"
+    fp8 = args.weights in ("fp8", "w8a8") and w.dtype == "bf16"
+    a8 = fp8 and args.weights == "w8a8"
     if fp8:
         # FP8 codes and per-row scales made on the device by the library's quantiser; the bf16
         # copies are freed before any timing
@@ -507,7 +511,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         wargs = (dev["w_gate_q"], dev["w_gate_s"], dev["w_up_q"], dev["w_up_s"], dev["w_down_q"], dev["w_down_s"])
-        forward, forward_timed = moe.moe_layer_forward_fp8, moe.moe_layer_forward_fp8_timed
+        forward, forward_timed = ((moe.moe_layer_forward_w8a8, moe.moe_layer_forward_w8a8_timed) if a8 else
+                                  (moe.moe_layer_forward_fp8, moe.moe_layer_forward_fp8_timed))
     else:
         wargs = (dev["w_gate"], dev["w_up"], dev["w_down"])
         forward, forward_timed = moe.moe_layer_forward, moe.moe_layer_forward_timed
@@ -664,6 +669,9 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     # fraction of the burst rate is reported as well. The float32 layer's MLP runs on the CUDA
     # cores and is compared with their FMA rate.
     peaks, peak_src = load_peaks()
+    # the E4M3 x E4M3 tensor-core rate is twice the bf16 one (nominal dense 4.5 vs 2.25 PFLOP/s):
+    # W8A8 contractions are compared with twice the measured bf16 rate
+    tensor_mult = 2.0 if a8 else 1.0
     gemm_ms = float(stage[:, 2].mean())
     pair_ms = float((stage[:, 2] + stage[:, 3]).mean())
     long_run = max_ms >= 1000.0
@@ -673,23 +681,26 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
                 "kernel": "ffn_gateup_fma_kernel (float32, CUDA cores)",
                 "peak_source": "float32 FMA rate: 148 SMs x 128 lanes x 2 flops x 2.032 GHz"}
     else:
-        t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * tensor_mult * 1e12)
         t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
         if t_tensor >= t_bytes:
             achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
-            peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+            peak = tensor_mult * (peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"])
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac_of_burst": achieved / peaks["bf16_tflops"]}
+                    "frac_of_burst": achieved / (peaks["bf16_tflops"] * tensor_mult)}
         else:
             achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-        roof["kernel"] = ("grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
+        roof["kernel"] = ("grouped_gemm_w8a8_kernel<gate/up, E4M3 weights and activations, SwiGLU epilogue> "
+                          "(tcgen05 kind::f8f6f4)" if a8 else
+                          "grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
                           "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
         roof["peak_source"] = (f"{peak_src} copy bandwidth" if roof["bound"] == "hbm" else
-                               f"{peak_src} sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else
-                               f"{peak_src} burst")
+                               (("2 x " if a8 else "") + f"{peak_src} bf16 ") +
+                               (f"sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else "burst"))
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.name, "fp8" if fp8 else "bf16") if w.dtype == "bf16" else None
+    roof["traffic"] = (measured_traffic(w.name, "w8a8" if a8 else "fp8" if fp8 else "bf16")
+                       if w.dtype == "bf16" else None)
     roof["ms_per_launch"] = gemm_ms
 
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
@@ -698,7 +709,7 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     weight_bytes = work["weight_bytes"]
     res = {
         "value": value, "ms_per_step": max_ms / K, "steps": K,
-        "config": config_of(w, kept, touched, world, "fp8" if fp8 else "bf16"),
+        "config": config_of(w, kept, touched, world, args.weights if fp8 else "bf16"),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": K2,
                 "copies": ("own streams, overlapping the neighbouring steps' layers (double-buffered)"
@@ -706,13 +717,13 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
                            % OVERLAP_MIN_BYTES),
                 "serial_value": whole_job_rate(w.T, K2, world, serial_ms),
                 "overlapped_value": whole_job_rate(w.T, K2, world, overlap_ms)},
-        "gpu_launches": K * moe.moe_layer_launch_count(cfg),
+        "gpu_launches": K * (moe.moe_layer_launch_count(cfg) + (1 if a8 else 0)),   # + the quantiser of h
         "roofline": roof,
         "clocks": clocks,
         "stages_ms": stages_ms,
         "stages_sum_ms": float(stage.sum(axis=1).mean()),
         "grouped_gemm_tflops": pair_flops / (pair_ms / 1e3) / 1e12,
-        "grouped_gemm_frac_of_burst": pair_flops / (pair_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "grouped_gemm_frac_of_burst": pair_flops / (pair_ms / 1e3) / 1e12 / (peaks["bf16_tflops"] * tensor_mult),
         "expert_weight_gbs": weight_bytes / (pair_ms / 1e3) / 1e9,
         "expert_weight_frac_of_hbm": weight_bytes / (pair_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
     }

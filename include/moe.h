@@ -298,6 +298,33 @@ moe_status_t moe_layer_forward_fp8_timed(const moe_config_t* cfg, const void* x,
                                          int32_t* counts_out, void* ws, size_t ws_bytes,
                                          void* const* events, int32_t n_events, cudaStream_t stream);
 
+/*
+ * The layer with FP8 (E4M3) expert weights AND E4M3 activations (W8A8). The source pages put
+ * the model's weights in FP8 (shubhamtatvamasi.com "Mixture of Experts", "Memory vs compute,
+ * quantified"); quantising the activations as well is this library's reading beyond them: the
+ * rows entering each expert contraction -- the grouped x rows before gate/up, and
+ * h = silu(g) * u (stored in bf16) before down -- are quantised per row exactly as the weights
+ * are (one float32 scale = max|row| / 448 per row, codes rounded to nearest even, saturated),
+ * and the contractions run on the 8-bit tensor-core path (tcgen05.mma kind::f8f6f4) with
+ * float32 accumulation; the row scales of both operands are applied to the accumulator. The
+ * results therefore differ from moe_layer_forward_fp8's by the activations' quantisation error
+ * (at most 2^-4 of an element). Arguments, layouts and errors as for moe_layer_forward_fp8;
+ * bf16 layers with d_model a multiple of 256 only (MOE_ERR_UNSUPPORTED otherwise). The
+ * grouping stage writes the grouped x rows as codes (no bf16 copy); one more kernel than
+ * moe_layer_forward enqueues (the quantiser of h).
+ */
+moe_status_t moe_layer_forward_w8a8(const moe_config_t* cfg, const void* x, const void* w_router,
+                                    const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                    const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                    const float* wd_s, void* out, int32_t* topk_idx_out, int32_t* counts_out,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
+moe_status_t moe_layer_forward_w8a8_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                          const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                          const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                          const float* wd_s, void* out, int32_t* topk_idx_out,
+                                          int32_t* counts_out, void* ws, size_t ws_bytes,
+                                          void* const* events, int32_t n_events, cudaStream_t stream);
+
 /* Number of kernel launches one moe_layer_forward call enqueues for this configuration (-1 if invalid). */
 int32_t moe_layer_launch_count(const moe_config_t* cfg);
 

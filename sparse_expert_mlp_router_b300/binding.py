@@ -24,7 +24,7 @@ EXPORTS = [
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
     "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
     "moe_permute_noalloc", "moe_routing_stats", "moe_quantize_fp8_rows", "moe_grouped_ffn_fp8",
-    "moe_layer_forward_fp8", "moe_layer_forward_fp8_timed",
+    "moe_layer_forward_fp8", "moe_layer_forward_fp8_timed", "moe_layer_forward_w8a8", "moe_layer_forward_w8a8_timed",
 ]
 
 
@@ -103,6 +103,10 @@ def lib() -> ctypes.CDLL:
                                        _vp], i32),
             "moe_layer_forward_fp8_timed": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                              _vp, sz, ctypes.POINTER(_vp), i32, _vp], i32),
+            "moe_layer_forward_w8a8": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, sz,
+                                        _vp], i32),
+            "moe_layer_forward_w8a8_timed": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              _vp, sz, ctypes.POINTER(_vp), i32, _vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -299,3 +303,23 @@ def moe_layer_forward_fp8_timed(cfg, x, w_router, bias, wg_q, wg_s, wu_q, wu_s, 
                                              _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(out),
                                              _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws), ws.numel(), handles,
                                              len(events), _stream(stream)), "moe_layer_forward_fp8_timed")
+
+
+def moe_layer_forward_w8a8(cfg, x, w_router, bias, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, out, ws, topk_idx_out=None,
+                           counts_out=None, stream=None) -> None:
+    _check(lib().moe_layer_forward_w8a8(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(wg_q),
+                                        _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(out),
+                                        _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "moe_layer_forward_w8a8")
+
+
+def moe_layer_forward_w8a8_timed(cfg, x, w_router, bias, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, out, ws, events,
+                                 topk_idx_out=None, counts_out=None, stream=None) -> None:
+    for e in events:
+        if e.cuda_event == 0:
+            e.record()
+    handles = (_vp * len(events))(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_w8a8_timed(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(wg_q),
+                                              _ptr(wg_s), _ptr(wu_q), _ptr(wu_s), _ptr(wd_q), _ptr(wd_s), _ptr(out),
+                                              _ptr(topk_idx_out), _ptr(counts_out), _ptr(ws), ws.numel(), handles,
+                                              len(events), _stream(stream)), "moe_layer_forward_w8a8_timed")

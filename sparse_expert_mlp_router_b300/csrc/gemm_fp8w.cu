@@ -37,6 +37,7 @@
 // reads) disappears, and the freed memory deepens the code ring.
 #include <cuda_fp8.h>
 
+#include "fp8_quant.cuh"
 #include "gemm_common.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
@@ -514,48 +515,8 @@ __global__ void quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ w, in
                                          uint8_t* __restrict__ wq, float* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-    const __nv_bfloat16* src = w + r * cols;
-    float mx = 0.0f;
-    for (int c = lane * 8; c < cols; c += 256) {
-      const uint4 u = *reinterpret_cast<const uint4*>(src + c);
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mx = fmaxf(mx, fabsf(__uint_as_float(wd[i] << 16)));
-        mx = fmaxf(mx, fabsf(__uint_as_float(wd[i] & 0xFFFF0000u)));
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float s = __fdiv_rn(mx, 448.0f);
-    if (lane == 0) scale[r] = s;
-    for (int c = lane * 16; c < cols; c += 512) {
-      const uint4 a = *reinterpret_cast<const uint4*>(src + c);
-      const uint4 b = *reinterpret_cast<const uint4*>(src + c + 8);
-      const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      uint32_t out[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t pair = wd[2 * i + h];
-          float2 v = make_float2(__uint_as_float(pair << 16), __uint_as_float(pair & 0xFFFF0000u));
-          if (s > 0.0f) {
-            v.x = __fdiv_rn(v.x, s);
-            v.y = __fdiv_rn(v.y, s);
-          } else {
-            v = make_float2(0.0f, 0.0f);
-          }
-          const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-          word |= (uint32_t)q << (16 * h);
-        }
-        out[i] = word;
-      }
-      *reinterpret_cast<uint4*>(wq + r * cols + c) = make_uint4(out[0], out[1], out[2], out[3]);
-    }
-  }
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps)
+    quantize_row_e4m3_warp(w + r * cols, cols, wq + r * cols, scale + r, lane);
 }
 
 // Resident-token tiles where the average expert holds at most 8 pairs (decode) and the tile's

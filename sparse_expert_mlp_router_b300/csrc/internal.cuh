@@ -27,10 +27,15 @@ struct WsLayout {
   size_t sched;         // [4*(G+1)] int32: group schedule of the grouped GEMMs
   size_t dest_row;      // [T*k] int32
   size_t src_token;     // [R] int32
-  size_t x_perm;        // [R*d] elements
+  size_t x_perm;        // [R*d] elements (at least T*d bytes: the W8A8 per-token codes)
   size_t h;             // [(R+S*T)*F] elements: silu(gate) * up
   size_t y;             // [(R+S*T)*d] elements: expert outputs; with the fused combine, the
-                        // [T*d] float32 output accumulator instead (the region holds either)
+                        // [T*d] float32 output accumulator instead (the region holds either);
+                        // in the W8A8 layer first the E4M3 codes of the expert inputs [(R+S*T)*d]
+  size_t a8_scale;      // [R+S*T] float: W8A8 per-row scales of the expert inputs
+  size_t xq_scale;      // [T] float: W8A8 per-token scales (the per-token codes use the x_perm region)
+  size_t h8;            // [(R+S*T)*F] bytes: W8A8 E4M3 codes of h
+  size_t h8_scale;      // [R+S*T] float: their per-row scales
   size_t total;
 };
 
@@ -138,6 +143,24 @@ cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const vo
                                     void* h, int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* wd_q, const float* wd_s,
                                   const void* sched, void* y, int32_t* status, cudaStream_t st);
+
+// W8A8 (E4M3 weights and activations, gemm_w8a8.cu).
+bool w8a8_supported(const Shape& s);
+// Activation rows to E4M3 codes + per-row scales: rows [0, min(*n_a, max_a)) of src_a to the
+// same rows of dst, rows [0, n_b) of src_b (may be NULL when n_b = 0) to rows [R, R + n_b).
+cudaError_t launch_quantize_act_rows(const Shape& s, const void* src_a, const int32_t* n_a, int64_t max_a,
+                                     const void* src_b, int64_t n_b, int cols, uint8_t* dst, float* scale,
+                                     cudaStream_t st);
+// x rows of the grouping (src_token order; the shared expert's tokens after row R) -> E4M3
+// codes and per-row scales, in place of the bf16 row copy. xq [T, d] bytes and xq_scale [T]:
+// scratch for the per-token codes of multi-chunk batches.
+cudaError_t launch_gather_quant_rows(const Shape& s, const void* x, const int32_t* src_token, const int32_t* offsets,
+                                     uint8_t* x8, float* x8_scale, uint8_t* xq, float* xq_scale, cudaStream_t st);
+cudaError_t launch_gemm_gateup_w8a8(const Shape& s, const uint8_t* x8, const float* x8_scale, const uint8_t* wg_q,
+                                    const float* wg_s, const uint8_t* wu_q, const float* wu_s, const void* sched,
+                                    void* h, int32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_down_w8a8(const Shape& s, const uint8_t* h8, const float* h8_scale, const uint8_t* wd_q,
+                                  const float* wd_s, const void* sched, void* y, int32_t* status, cudaStream_t st);
 
 cudaError_t launch_combine(const Shape& s, const void* y, const int32_t* dest_row,
                            const float* gate, void* out, int32_t* status, cudaStream_t st);

@@ -117,11 +117,20 @@ WsLayout make_layout(const Shape& s) {
   L.sched = take((size_t)4 * (s.G + 1) * 4);
   L.dest_row = take(pairs * 4);
   L.src_token = take((size_t)s.R * 4);
-  L.x_perm = take((size_t)s.R * s.d * s.esize);
+  // x_perm also holds the W8A8 layer's per-token codes [T, d] (bytes)
+  size_t xp_bytes = (size_t)s.R * s.d * s.esize;
+  if (s.dtype == MOE_BF16 && xp_bytes < (size_t)s.T * s.d) xp_bytes = (size_t)s.T * s.d;
+  L.x_perm = take(xp_bytes);
   L.h = take(grouped * s.F * s.esize);
   size_t y_bytes = grouped * s.d * s.esize;
   if (s.dtype == MOE_BF16 && y_bytes < (size_t)s.T * s.d * 4) y_bytes = (size_t)s.T * s.d * 4;   // fused combine
   L.y = take(y_bytes);
+  if (s.dtype == MOE_BF16) {
+    L.a8_scale = take(grouped * 4);
+    L.xq_scale = take((size_t)s.T * 4);
+    L.h8 = take(grouped * s.F);
+    L.h8_scale = take(grouped * 4);
+  }
   L.total = o;
   return L;
 }
@@ -164,9 +173,11 @@ cudaError_t run_router(const Shape& s, const void* x, const void* w_router, cons
 
 // with_schedule: the scan also builds the group schedule of the grouped GEMMs (the
 // whole-layer call); the permute stage call leaves it to moe_grouped_ffn.
+// x8 / x8s (W8A8 layer): when set, the grouped rows are written as E4M3 codes with per-row
+// scales (the shared expert's tokens after row R) instead of the bf16 copy in x_perm.
 cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx, const void* x,
                         int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_token, void* x_perm,
-                        bool with_schedule, cudaStream_t st) {
+                        bool with_schedule, cudaStream_t st, uint8_t* x8 = nullptr, float* x8s = nullptr) {
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
   cudaError_t e;
@@ -174,13 +185,16 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
     if ((e = launch_group_single_chunk(s, idx, counts, offsets, dest_row, src_token,
                                        with_schedule ? at<void>(ws, L.sched) : nullptr, status, st)) != cudaSuccess)
       return e;
-    return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
+  } else {
+    if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
+    if ((e = launch_group_scan(s, cc, counts, offsets, with_schedule ? at<void>(ws, L.sched) : nullptr, st)) !=
+        cudaSuccess)
+      return e;
+    if ((e = launch_group_scatter(s, idx, cc, offsets, dest_row, src_token, st)) != cudaSuccess) return e;
   }
-  if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
-  if ((e = launch_group_scan(s, cc, counts, offsets, with_schedule ? at<void>(ws, L.sched) : nullptr, st)) !=
-      cudaSuccess)
-    return e;
-  if ((e = launch_group_scatter(s, idx, cc, offsets, dest_row, src_token, st)) != cudaSuccess) return e;
+  if (x8 != nullptr)   // per-token codes (multi-chunk batches) go to the unused x_perm region
+    return launch_gather_quant_rows(s, x, src_token, offsets, x8, x8s, static_cast<uint8_t*>(x_perm),
+                                    at<float>(ws, L.xq_scale), st);
   return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
 }
 
@@ -198,6 +212,7 @@ struct ExpertWeights {
   const float* us = nullptr;
   const float* ds = nullptr;
   bool fp8 = false;
+  bool a8 = false;       // W8A8: the activations entering each contraction quantised to E4M3 too
 };
 
 cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const void* x,
@@ -267,6 +282,7 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   if (w.fp8 && (rc = check_fp8_weights(s, static_cast<const uint8_t*>(w.g), w.gs, static_cast<const uint8_t*>(w.u),
                                        w.us, static_cast<const uint8_t*>(w.d), w.ds)) != MOE_OK)
     return rc;
+  if (w.a8 && !w8a8_supported(s)) return MOE_ERR_UNSUPPORTED;
   if ((rc = check_ws(s, ws, ws_bytes)) != MOE_OK) return rc;
   const WsLayout L = make_layout(s);
   cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
@@ -292,7 +308,12 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   if (!mark(1)) return MOE_ERR_CUDA;
   {
     const NvtxRange r("moe_layer/grouping");
-    if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st) != cudaSuccess)
+    // W8A8: the grouped x rows go straight to E4M3 codes in the y region (free until the down
+    // projection writes y)
+    uint8_t* x8 = w.a8 ? at<uint8_t>(ws, L.y) : nullptr;
+    float* x8s = w.a8 ? at<float>(ws, L.a8_scale) : nullptr;
+    if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st, x8, x8s) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if (!mark(2)) return MOE_ERR_CUDA;
@@ -300,7 +321,27 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   float* acc = at<float>(ws, L.y);
   {
     const NvtxRange r("moe_layer/experts");
-    if (fused) {
+    if (w.a8) {
+      // gate/up on the codes of the grouping stage, h -> codes, down on codes
+      void* sched = at<void>(ws, L.sched);
+      void* h = at<void>(ws, L.h);
+      uint8_t* x8 = at<uint8_t>(ws, L.y);
+      float* x8s = at<float>(ws, L.a8_scale);
+      uint8_t* h8 = at<uint8_t>(ws, L.h8);
+      float* h8s = at<float>(ws, L.h8_scale);
+      const int64_t n_sh = (int64_t)s.S * s.T;
+      if (launch_gemm_gateup_w8a8(s, x8, x8s, static_cast<const uint8_t*>(w.g), w.gs, static_cast<const uint8_t*>(w.u),
+                                  w.us, sched, h, status, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (!mark(3)) return MOE_ERR_CUDA;
+      const void* h_shared = n_sh ? static_cast<const void*>(static_cast<const char*>(h) + (size_t)s.R * s.F * 2)
+                                  : nullptr;
+      if (launch_quantize_act_rows(s, h, offsets + s.E, s.R, h_shared, n_sh, s.F, h8, h8s, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (launch_gemm_down_w8a8(s, h8, h8s, static_cast<const uint8_t*>(w.d), w.ds, sched, y, status, st) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (fused) {
       void* sched = at<void>(ws, L.sched);
       void* h = at<void>(ws, L.h);
       if (launch_gemm_gateup_tc(s, x_perm, x, w.g, w.u, sched, h, status, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -463,6 +504,24 @@ moe_status_t moe_layer_forward_fp8_timed(const moe_config_t* cfg, const void* x,
                                          void* ws, size_t ws_bytes, void* const* events, int32_t n_events,
                                          cudaStream_t stream) {
   return layer_forward(cfg, x, w_router, bias, ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true}, out,
+                       topk_idx_out, counts_out, ws, ws_bytes, events, n_events, stream);
+}
+
+moe_status_t moe_layer_forward_w8a8(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
+                                    const uint8_t* wg_q, const float* wg_s, const uint8_t* wu_q, const float* wu_s,
+                                    const uint8_t* wd_q, const float* wd_s, void* out, int32_t* topk_idx_out,
+                                    int32_t* counts_out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true, true}, out,
+                       topk_idx_out, counts_out, ws, ws_bytes, nullptr, 0, stream);
+}
+
+moe_status_t moe_layer_forward_w8a8_timed(const moe_config_t* cfg, const void* x, const void* w_router,
+                                          const float* bias, const uint8_t* wg_q, const float* wg_s,
+                                          const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                          const float* wd_s, void* out, int32_t* topk_idx_out, int32_t* counts_out,
+                                          void* ws, size_t ws_bytes, void* const* events, int32_t n_events,
+                                          cudaStream_t stream) {
+  return layer_forward(cfg, x, w_router, bias, ExpertWeights{wg_q, wu_q, wd_q, wg_s, wu_s, wd_s, true, true}, out,
                        topk_idx_out, counts_out, ws, ws_bytes, events, n_events, stream);
 }
 

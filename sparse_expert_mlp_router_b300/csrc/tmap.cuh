@@ -59,4 +59,21 @@ inline bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
+// 2D map over a row-major byte tensor [rows, inner] (E4M3 codes) in the layout the 8-bit
+// tensor-core MMA reads: box {128, box_rows} (128 codes = one 128-byte swizzle atom along the
+// contiguous dimension), 128-byte swizzle, zero fill outside the tensor. `inner` must make a
+// row a multiple of 16 bytes.
+inline bool make_tmap_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = tmap_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace moe

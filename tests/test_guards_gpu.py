@@ -126,3 +126,19 @@ def test_fp8_layer_and_quantiser_write_only_their_outputs():
                               bufs["out"].t, bufs["workspace"].t)
     assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
     _check_all(bufs, "fp8 layer")
+
+
+@pytest.mark.parametrize("name,edit", [("mini_qwen3", {"T": 200}), ("mini_deepseek", {"capacity_factor": 0.05}),
+                                       ("mini_decode", {})])
+def test_w8a8_layer_writes_only_its_outputs(name, edit):
+    # the W8A8 layer keeps its codes and scales inside the workspace (per-token codes in the
+    # x_perm region, grouped codes in the y region), also when capacity makes R smaller than T
+    w = synth.WORKLOADS[name].with_(**edit)
+    dev = Inputs(w).device()
+    cfg = cfg_of(w)
+    q = {n: moe.moe_quantize_fp8_rows(dev[n]) for n in ("w_gate", "w_up", "w_down")}
+    bufs = {"out": Guarded((w.T, w.d_model), torch.bfloat16), "workspace": _workspace(cfg)}
+    moe.moe_layer_forward_w8a8(cfg, dev["x"], dev["w_router"], dev["bias"], *q["w_gate"], *q["w_up"], *q["w_down"],
+                               bufs["out"].t, bufs["workspace"].t)
+    assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
+    _check_all(bufs, f"w8a8 layer {name}")
