@@ -97,6 +97,9 @@ def parse_args(argv=None):
     ap.add_argument("--combine", choices=["separate", "fused"], default="separate",
                     help="combine as its own kernel (default), or fused into the down projection's "
                          "epilogue as float32 reductions (sets MOE_FUSED_COMBINE=1)")
+    ap.add_argument("--no-w8a8", action="store_true",
+                    help="skip the W8A8 (E4M3 weights and activations) measurement of each bf16 workload that "
+                         "the default multi-workload line adds under 'w8a8'")
     ap.add_argument("--eager", action="store_true",
                     help="time K separate launches of the layer instead of CUDA-graph replays")
     return ap.parse_args(argv)
@@ -483,9 +486,12 @@ def staged_positions(K: int) -> list:
     return [((j + 1) * K) // n - 1 for j in range(n)]
 
 
-def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
+def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights: str = None,
+                     with_e2e: bool = True) -> dict:
     """Everything the bench reports for one workload: device-timed value, stage times, roofline,
-    end-to-end rate, clocks and (rank 0, N = 1) the CPU oracle baseline."""
+    end-to-end rate (with_e2e), clocks and (rank 0, N = 1) the CPU oracle baseline. weights:
+    bf16, fp8 or w8a8 (default: --weights)."""
+    weights = args.weights if weights is None else weights
     import numpy as np
     import torch
     import synth
@@ -500,8 +506,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
                           n_shared=w.n_shared, score=w.score, renormalize=w.renormalize,
                           capacity_factor=w.capacity_factor, dtype=w.dtype)
     dev = synth.device_inputs(w)
-    fp8 = args.weights in ("fp8", "w8a8") and w.dtype == "bf16"
-    a8 = fp8 and args.weights == "w8a8"
+    fp8 = weights in ("fp8", "w8a8") and w.dtype == "bf16"
+    a8 = fp8 and weights == "w8a8"
     if fp8:
         # FP8 codes and per-row scales made on the device by the library's quantiser; the bf16
         # copies are freed before any timing
@@ -587,81 +593,91 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     value = whole_job_rate(w.T, K, world, max_ms)
     del graph
 
-    # end to end: activations in pinned host memory, copies inside the timed region. Two loops:
-    # serial (one stream: copy x in, run the layer, copy the output out), and overlapped (the
-    # copies on their own streams, two device buffers of each, so that step i's copies overlap
-    # the layers of steps i-1 and i+1). Cross-stream waits cost a few microseconds a step, more
-    # than copies of a few hundred KB take, so the reported loop is the overlapped one when a
-    # step's activations reach OVERLAP_MIN_BYTES and the serial one below; both are reported.
-    x_host = dev["x"].cpu().pin_memory()
-    out_hosts = [torch.empty(out.shape, dtype=dt).pin_memory() for _ in range(2)]
-    x_devs = [torch.empty_like(dev["x"]) for _ in range(2)]
-    out_devs = [out, torch.empty_like(out)]
-    main = torch.cuda.current_stream()
-    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # x_devs[b] holds this step's input
-    ev_done = [torch.cuda.Event() for _ in range(2)]    # the layer on buffer pair b finished
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # out_devs[b] copied to the host
+    e2e = None
+    if with_e2e:
+        # end to end: activations in pinned host memory, copies inside the timed region. Two loops:
+        # serial (one stream: copy x in, run the layer, copy the output out), and overlapped (the
+        # copies on their own streams, two device buffers of each, so that step i's copies overlap
+        # the layers of steps i-1 and i+1). Cross-stream waits cost a few microseconds a step, more
+        # than copies of a few hundred KB take, so the reported loop is the overlapped one when a
+        # step's activations reach OVERLAP_MIN_BYTES and the serial one below; both are reported.
+        x_host = dev["x"].cpu().pin_memory()
+        out_hosts = [torch.empty(out.shape, dtype=dt).pin_memory() for _ in range(2)]
+        x_devs = [torch.empty_like(dev["x"]) for _ in range(2)]
+        out_devs = [out, torch.empty_like(out)]
+        main = torch.cuda.current_stream()
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]      # x_devs[b] holds this step's input
+        ev_done = [torch.cuda.Event() for _ in range(2)]    # the layer on buffer pair b finished
+        ev_out = [torch.cuda.Event() for _ in range(2)]     # out_devs[b] copied to the host
 
-    def e2e_step(i):
-        b = i % 2
-        h2d.wait_event(ev_done[b])                       # the layer that read x_devs[b] is done
-        with torch.cuda.stream(h2d):
-            x_devs[b].copy_(x_host, non_blocking=True)
-        ev_in[b].record(h2d)
-        main.wait_event(ev_in[b])
-        main.wait_event(ev_out[b])                       # out_devs[b] is free again
-        forward(cfg, x_devs[b], dev["w_router"], dev["bias"], *wargs, out_devs[b], ws)
-        ev_done[b].record(main)
-        d2h.wait_event(ev_done[b])
-        with torch.cuda.stream(d2h):
-            out_hosts[b].copy_(out_devs[b], non_blocking=True)
-        ev_out[b].record(d2h)
+        def e2e_step(i):
+            b = i % 2
+            h2d.wait_event(ev_done[b])                       # the layer that read x_devs[b] is done
+            with torch.cuda.stream(h2d):
+                x_devs[b].copy_(x_host, non_blocking=True)
+            ev_in[b].record(h2d)
+            main.wait_event(ev_in[b])
+            main.wait_event(ev_out[b])                       # out_devs[b] is free again
+            forward(cfg, x_devs[b], dev["w_router"], dev["bias"], *wargs, out_devs[b], ws)
+            ev_done[b].record(main)
+            d2h.wait_event(ev_done[b])
+            with torch.cuda.stream(d2h):
+                out_hosts[b].copy_(out_devs[b], non_blocking=True)
+            ev_out[b].record(d2h)
 
-    def e2e_serial_step():
-        x_devs[0].copy_(x_host, non_blocking=True)
-        forward(cfg, x_devs[0], dev["w_router"], dev["bias"], *wargs, out_devs[0], ws)
-        out_hosts[0].copy_(out_devs[0], non_blocking=True)
+        def e2e_serial_step():
+            x_devs[0].copy_(x_host, non_blocking=True)
+            forward(cfg, x_devs[0], dev["w_router"], dev["bias"], *wargs, out_devs[0], ws)
+            out_hosts[0].copy_(out_devs[0], non_blocking=True)
 
-    # By default each loop is warmed up for E2E_WARM_S of wall time (the host's clock settles: a
-    # cold host doubled the per-step cost of the smallest layers) and timed over at least
-    # E2E_MIN_S of steps; --e2e-steps N times exactly N steps after a few warm-up steps.
-    auto = args.e2e_steps is None
-    K2 = max(100, math.ceil(E2E_MIN_S / (max_ms / K / 1e3))) if auto else max(args.e2e_steps, 1)
+        # By default each loop is warmed up for E2E_WARM_S of wall time (the host's clock settles: a
+        # cold host doubled the per-step cost of the smallest layers) and timed over at least
+        # E2E_MIN_S of steps; --e2e-steps N times exactly N steps after a few warm-up steps.
+        auto = args.e2e_steps is None
+        K2 = max(100, math.ceil(E2E_MIN_S / (max_ms / K / 1e3))) if auto else max(args.e2e_steps, 1)
 
-    def warm(fn, n_min):
-        t_end = time.perf_counter() + (E2E_WARM_S if auto else 0.0)
-        i = 0
-        while i < n_min or time.perf_counter() < t_end:
-            fn(i)
-            i += 1
-        torch.cuda.synchronize()
+        def warm(fn, n_min):
+            t_end = time.perf_counter() + (E2E_WARM_S if auto else 0.0)
+            i = 0
+            while i < n_min or time.perf_counter() < t_end:
+                fn(i)
+                i += 1
+            torch.cuda.synchronize()
 
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    warm(lambda i: e2e_serial_step(), 3)
-    barrier()
-    e0.record()
-    for i in range(K2):
-        e2e_serial_step()
-    e1.record()
-    barrier()
-    serial_ms = max_over_ranks(e0.elapsed_time(e1), dist)
-    warm(e2e_step, 4)                                    # the two loops share buffer 0: synchronised
-    barrier()
-    e0.record()
-    h2d.wait_stream(main)
-    d2h.wait_stream(main)
-    for i in range(K2):
-        e2e_step(i)
-    main.wait_stream(d2h)                                # the last output has reached the host
-    e1.record()
-    barrier()
-    overlap_ms = max_over_ranks(e0.elapsed_time(e1), dist)
-    overlapped = x_host.numel() * x_host.element_size() >= OVERLAP_MIN_BYTES
-    e2e_value = whole_job_rate(w.T, K2, world, overlap_ms if overlapped else serial_ms)
-    if moe.moe_get_device_error(ws) != moe.MOE_OK:
-        raise RuntimeError(f"{w.name}: device status after e2e timing")
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        warm(lambda i: e2e_serial_step(), 3)
+        barrier()
+        e0.record()
+        for i in range(K2):
+            e2e_serial_step()
+        e1.record()
+        barrier()
+        serial_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+        warm(e2e_step, 4)                                    # the two loops share buffer 0: synchronised
+        barrier()
+        e0.record()
+        h2d.wait_stream(main)
+        d2h.wait_stream(main)
+        for i in range(K2):
+            e2e_step(i)
+        main.wait_stream(d2h)                                # the last output has reached the host
+        e1.record()
+        barrier()
+        overlap_ms = max_over_ranks(e0.elapsed_time(e1), dist)
+        overlapped = x_host.numel() * x_host.element_size() >= OVERLAP_MIN_BYTES
+        e2e_value = whole_job_rate(w.T, K2, world, overlap_ms if overlapped else serial_ms)
+        if moe.moe_get_device_error(ws) != moe.MOE_OK:
+            raise RuntimeError(f"{w.name}: device status after e2e timing")
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+               "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": K2,
+               "copies": ("own streams, overlapping the neighbouring steps' layers (double-buffered)"
+                          if overlapped else "serial, on the layer's stream (activations under %d bytes)"
+                          % OVERLAP_MIN_BYTES),
+               "serial_value": whole_job_rate(w.T, K2, world, serial_ms),
+               "overlapped_value": whole_job_rate(w.T, K2, world, overlap_ms)}
+        del x_host, out_hosts, x_devs, out_devs
 
     # roofline of the dominant kernel: the gate/up grouped GEMM (stage 2 -> 3). A tensor-bound
     # kernel timed inside a long run of back-to-back layers (>= 1 s, where the GPU settles at
@@ -709,14 +725,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
     weight_bytes = work["weight_bytes"]
     res = {
         "value": value, "ms_per_step": max_ms / K, "steps": K,
-        "config": config_of(w, kept, touched, world, args.weights if fp8 else "bf16"),
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-                "d2h_bytes_per_step": int(out.numel() * out.element_size()), "steps": K2,
-                "copies": ("own streams, overlapping the neighbouring steps' layers (double-buffered)"
-                           if overlapped else "serial, on the layer's stream (activations under %d bytes)"
-                           % OVERLAP_MIN_BYTES),
-                "serial_value": whole_job_rate(w.T, K2, world, serial_ms),
-                "overlapped_value": whole_job_rate(w.T, K2, world, overlap_ms)},
+        "config": config_of(w, kept, touched, world, weights if fp8 else "bf16"),
+        "e2e": e2e,
         "gpu_launches": K * (moe.moe_layer_launch_count(cfg) + (1 if a8 else 0)),   # + the quantiser of h
         "roofline": roof,
         "clocks": clocks,
@@ -727,7 +737,7 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool) -> dict:
         "expert_weight_gbs": weight_bytes / (pair_ms / 1e3) / 1e9,
         "expert_weight_frac_of_hbm": weight_bytes / (pair_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
     }
-    del dev, ws, out, counts, x_host, out_hosts, x_devs, out_devs, wargs, args_fwd
+    del dev, ws, out, counts, wargs, args_fwd
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     if with_cpu:
@@ -751,11 +761,19 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    import synth
     head = measure_workload(args, w, dist, local, rank, world, with_cpu)
     extras = {}
     for name in extra_workloads(args):
-        import synth
         extras[name] = measure_workload(args, synth.WORKLOADS[name], dist, local, rank, world, with_cpu)
+    # the FP8 path (E4M3 weights and activations) on every bf16 workload of the line: device-timed
+    # value, stages and roofline only
+    if args.weights == "bf16" and not args.no_w8a8 and extras:
+        for name, res in [(w.name, head)] + list(extras.items()):
+            wl = synth.WORKLOADS[name]
+            if wl.dtype == "bf16":
+                res["w8a8"] = measure_workload(args, wl, dist, local, rank, world, False, weights="w8a8",
+                                               with_e2e=False)
     line = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
@@ -767,6 +785,8 @@ def run_ours(args, w):
         "grouped_gemm_frac_of_burst": head["grouped_gemm_frac_of_burst"],
         "expert_weight_frac_of_hbm": head["expert_weight_frac_of_hbm"],
     }
+    if "w8a8" in head:
+        line["w8a8"] = head["w8a8"]
     if extras:
         line["workloads"] = extras
     if rank == 0:
