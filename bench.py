@@ -91,6 +91,8 @@ def parse_args(argv=None):
     ap.add_argument("--weights", choices=["bf16", "fp8", "w8a8"], default="bf16",
                     help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales (fp8), or "
                          "those weights with the expert inputs quantised to E4M3 per row as well (w8a8)")
+    ap.add_argument("--traffic-kind", choices=["bf16", "fp8", "w8a8", "fused"], default=None,
+                    help="with --write-traffic: which kernels the CSVs hold (default: --weights)")
     ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
                     help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
                          "write_traffic) and exit")
@@ -211,6 +213,7 @@ class ClockSampler:
 
 
 GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh"),
+                "fused": ("gemm_fused.cu", "epilogue.cuh", "gemm_common.cuh", "tc_ptx.cuh"),
                 "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh"),
                 "w8a8": ("gemm_w8a8.cu", "fp8_quant.cuh", "gemm_common.cuh", "tc_ptx.cuh")}
 
@@ -255,8 +258,9 @@ def write_traffic(csv_dir: str, weights: str) -> None:
             python bench.py --workload <workload> --steps 3 --warmup 1 --e2e-steps 1 --no-cpu-baseline \\
             --eager [--weights fp8]
 
-    (the second layer forward's gate/up and down GEMMs). Each entry records the hash of the GEMM
-    source it was measured on; the roofline reports the traffic only while that source is unchanged.
+    (the second layer forward's gate/up and down GEMMs; with --weights fused, -k regex:grouped_mlp_fused -c 1 on a
+    layer that runs the expert MLP as one launch). Each entry records the hash of the GEMM source it was measured
+    on; the roofline reports the traffic only while that source is unchanged.
     """
     import csv
     import glob
@@ -270,13 +274,15 @@ def write_traffic(csv_dir: str, weights: str) -> None:
         per = {}
         for r in rows[1:]:
             per.setdefault(r[ids], {"k": r[ki]})[r[mi]] = float(r[vi].replace(",", ""))
-        gu, dn = list(per.values())[:2]            # gate/up is launched before down
+        gu = list(per.values())[0]                 # gate/up is launched before down
         key = wl if weights == "bf16" else wl + "+" + weights
         out[key] = {"source_sha256": sha, "kernel": gu["k"][:60],
                     "bytes_per_launch": gu["dram__bytes_read.sum"] + gu["dram__bytes_write.sum"],
                     "read": gu["dram__bytes_read.sum"], "write": gu["dram__bytes_write.sum"],
-                    "ns_under_ncu": gu["gpu__time_duration.sum"],
-                    "down_bytes_per_launch": dn["dram__bytes_read.sum"] + dn["dram__bytes_write.sum"]}
+                    "ns_under_ncu": gu["gpu__time_duration.sum"]}
+        if weights != "fused":                      # the one-launch MLP has no separate down kernel
+            dn = list(per.values())[1]
+            out[key]["down_bytes_per_launch"] = dn["dram__bytes_read.sum"] + dn["dram__bytes_write.sum"]
     out["_comment"] = ("DRAM bytes per launch of the gate/up grouped GEMM (and of the down GEMM) from one-pass ncu "
                        "captures; written by `python bench.py --write-traffic DIR`, see write_traffic().")
     with open(TRAFFIC_FILE, "w") as f:
@@ -684,30 +690,37 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
     # its power limit) is compared with the sustained bf16 rate, else with the burst rate; the
     # fraction of the burst rate is reported as well. The float32 layer's MLP runs on the CUDA
     # cores and is compared with their FMA rate.
+    # the bf16 layer's expert MLP may run as one launch of both contractions (decode-shaped
+    # batches): then the dominant kernel is that launch, timed over both stages, with the flops
+    # and bytes of both contractions
+    one_mlp = (not fp8) and w.dtype == "bf16" and moe.moe_layer_mlp_fused(cfg) == 1
     peaks, peak_src = load_peaks()
     # the E4M3 x E4M3 tensor-core rate is twice the bf16 one (nominal dense 4.5 vs 2.25 PFLOP/s):
     # W8A8 contractions are compared with twice the measured bf16 rate
     tensor_mult = 2.0 if a8 else 1.0
-    gemm_ms = float(stage[:, 2].mean())
     pair_ms = float((stage[:, 2] + stage[:, 3]).mean())
+    gemm_ms = pair_ms if one_mlp else float(stage[:, 2].mean())
+    r_flops = work["gateup_flops"] + (work["down_flops"] if one_mlp else 0.0)
+    r_bytes = work["gateup_bytes"] + (work["down_bytes"] if one_mlp else 0.0)
     long_run = max_ms >= 1000.0
     if w.dtype != "bf16":
-        achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
+        achieved = r_flops / (gemm_ms / 1e3) / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": F32_FMA_TFLOPS, "unit": "TFLOP/s",
                 "kernel": "ffn_gateup_fma_kernel (float32, CUDA cores)",
                 "peak_source": "float32 FMA rate: 148 SMs x 128 lanes x 2 flops x 2.032 GHz"}
     else:
-        t_tensor = work["gateup_flops"] / (peaks["bf16_tflops"] * tensor_mult * 1e12)
-        t_bytes = work["gateup_bytes"] / (peaks["hbm_gbs"] * 1e9)
+        t_tensor = r_flops / (peaks["bf16_tflops"] * tensor_mult * 1e12)
+        t_bytes = r_bytes / (peaks["hbm_gbs"] * 1e9)
         if t_tensor >= t_bytes:
-            achieved = work["gateup_flops"] / (gemm_ms / 1e3) / 1e12
+            achieved = r_flops / (gemm_ms / 1e3) / 1e12
             peak = tensor_mult * (peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"])
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac_of_burst": achieved / (peaks["bf16_tflops"] * tensor_mult)}
         else:
-            achieved = work["gateup_bytes"] / (gemm_ms / 1e3) / 1e9
+            achieved = r_bytes / (gemm_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-        roof["kernel"] = ("grouped_gemm_w8a8_kernel<gate/up, E4M3 weights and activations, SwiGLU epilogue> "
+        roof["kernel"] = ("grouped_mlp_fused_kernel<gate/up + SwiGLU, then down, one launch> (tcgen05)" if one_mlp else
+                          "grouped_gemm_w8a8_kernel<gate/up, E4M3 weights and activations, SwiGLU epilogue> "
                           "(tcgen05 kind::f8f6f4)" if a8 else
                           "grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
                           "grouped_gemm_kernel<gate/up, SwiGLU epilogue> (tcgen05)")
@@ -715,7 +728,7 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
                                (("2 x " if a8 else "") + f"{peak_src} bf16 ") +
                                (f"sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else "burst"))
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = (measured_traffic(w.name, "w8a8" if a8 else "fp8" if fp8 else "bf16")
+    roof["traffic"] = (measured_traffic(w.name, "fused" if one_mlp else "w8a8" if a8 else "fp8" if fp8 else "bf16")
                        if w.dtype == "bf16" else None)
     roof["ms_per_launch"] = gemm_ms
 
@@ -727,7 +740,10 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
         "value": value, "ms_per_step": max_ms / K, "steps": K,
         "config": config_of(w, kept, touched, world, weights if fp8 else "bf16"),
         "e2e": e2e,
-        "gpu_launches": K * (moe.moe_layer_launch_count(cfg) + (1 if a8 else 0)),   # + the quantiser of h
+        # moe_layer_launch_count counts the bf16 layer; the FP8 layers run the expert MLP as two
+        # launches, and W8A8 adds the quantiser of h
+        "gpu_launches": K * (moe.moe_layer_launch_count(cfg) + (moe.moe_layer_mlp_fused(cfg) if fp8 else 0)
+                             + (1 if a8 else 0)),
         "roofline": roof,
         "clocks": clocks,
         "stages_ms": stages_ms,
@@ -798,7 +814,7 @@ def run_ours(args, w):
 def main():
     args = parse_args()
     if args.write_traffic:
-        write_traffic(args.write_traffic, args.weights)
+        write_traffic(args.write_traffic, args.traffic_kind or args.weights)
         return
     import synth
     w = synth.WORKLOADS[args.workload]

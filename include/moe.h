@@ -325,8 +325,24 @@ moe_status_t moe_layer_forward_w8a8_timed(const moe_config_t* cfg, const void* x
                                           int32_t* counts_out, void* ws, size_t ws_bytes,
                                           void* const* events, int32_t n_events, cudaStream_t stream);
 
-/* Number of kernel launches one moe_layer_forward call enqueues for this configuration (-1 if invalid). */
+/* Number of kernel launches one moe_layer_forward call (bf16 or float32 weights) enqueues for this
+ * configuration (-1 if invalid). The FP8-weight layer launches two expert-MLP kernels where
+ * moe_layer_mlp_fused reports one, and the W8A8 layer one more (the quantiser of h). */
 int32_t moe_layer_launch_count(const moe_config_t* cfg);
+
+/*
+ * 1 if moe_layer_forward runs the expert MLP's two contractions (gate/up + SwiGLU, then down)
+ * as one persistent launch for this configuration, 0 if as two, -1 if the configuration is
+ * invalid. One launch is the default for bf16 layers whose batch is a single chunk of at most
+ * 128 tokens (decode): each CTA takes its gate/up tiles, then its down tiles, and a down tile
+ * waits (bounded) until every gate/up tile of its 128-row block has published its rows of h
+ * through a counter in the workspace. The results are bit-identical to the two launches.
+ * MOE_FUSED_MLP=1 or 0 in the environment forces one or two launches for every bf16 layer
+ * whose d_model is a multiple of 256 (read at every call). The one launch needs all of its
+ * CTAs (one per SM) resident at once: a GPU shared with other work that holds SMs for long can
+ * make its waits run out (MOE_ERR_TIMEOUT in the status word) instead of hanging.
+ */
+int32_t moe_layer_mlp_fused(const moe_config_t* cfg);
 
 /*
  * Synchronise `stream`, then return the first device-side status recorded in the workspace

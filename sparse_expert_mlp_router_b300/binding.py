@@ -22,7 +22,7 @@ EXPORTS = [
     "moe_status_string", "moe_check_config", "moe_capacity", "moe_rows_capacity", "moe_grouped_rows",
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
-    "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count",
+    "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count", "moe_layer_mlp_fused",
     "moe_permute_noalloc", "moe_routing_stats", "moe_quantize_fp8_rows", "moe_grouped_ffn_fp8",
     "moe_layer_forward_fp8", "moe_layer_forward_fp8_timed", "moe_layer_forward_w8a8", "moe_layer_forward_w8a8_timed",
 ]
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "moe_clear_device_error": ([_vp, _vp], i32),
             "moe_selftest_bounded_wait": ([_vp, sz, u64, _vp], i32),
             "moe_layer_launch_count": ([_cfgp], i32),
+            "moe_layer_mlp_fused": ([_cfgp], i32),
             "moe_permute_noalloc": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
             "moe_routing_stats": ([_cfgp, _vp, _vp, _vp], i32),
             "moe_quantize_fp8_rows": ([_vp, i64, i32, _vp, _vp, _vp], i32),
@@ -160,6 +161,10 @@ def moe_workspace_size(cfg: MoeConfig) -> int:
 
 def moe_layer_launch_count(cfg: MoeConfig) -> int:
     return lib().moe_layer_launch_count(ctypes.byref(cfg))
+
+
+def moe_layer_mlp_fused(cfg: MoeConfig) -> int:
+    return lib().moe_layer_mlp_fused(ctypes.byref(cfg))
 
 
 # -------------------------------------------------------------- workspace

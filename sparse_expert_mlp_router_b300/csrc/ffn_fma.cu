@@ -11,9 +11,9 @@
 // bounds.
 //
 // The float32 path computes the same SwiGLU expert MLP as the tensor-core
-// path, y = W_down (silu(W_gate a) * (W_up a)), one output element per thread
-// with float32 FMAs; tensor cores have no float32 mode precise enough for
-// float32 layers. It serves layers stored in float32.
+// path, y = W_down (silu(W_gate a) * (W_up a)), one output element per four
+// lanes with float32 FMAs; tensor cores have no float32 mode precise enough
+// for float32 layers. It serves layers stored in float32.
 #include "internal.cuh"
 #include "sched.cuh"
 
@@ -51,48 +51,87 @@ __device__ __forceinline__ int row_group(const int32_t* sched, int G, int64_t r,
   return -1;
 }
 
-template <typename TE>
-__global__ void ffn_gateup_fma_kernel(const TE* __restrict__ x_perm, const TE* __restrict__ x,
-                                      const TE* __restrict__ wg, const TE* __restrict__ wu,
+// Four lanes share one output element: lane part p of the quad takes the float4 vectors
+// v = p, p + 4, p + 8, ... of the reduction, so the quad's loads of a weight row are contiguous
+// (64 bytes per step) and a thread's chain of dependent FMAs is a quarter of the reduction; the
+// quad's partial sums are then added with two shuffles.
+constexpr int kQuad = 4;
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+
+__global__ void ffn_gateup_fma_kernel(const float* __restrict__ x_perm, const float* __restrict__ x,
+                                      const float* __restrict__ wg, const float* __restrict__ wu,
                                       const int32_t* __restrict__ sched, int G, int E, int d, int F,
-                                      int64_t n_rows, TE* __restrict__ h) {
+                                      int64_t n_rows, float* __restrict__ h) {
+  const int p = threadIdx.x & (kQuad - 1);
   const int64_t total = n_rows * F;
-  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = o / F;
-    const int f = (int)(o % F);
-    int local = 0;
-    const int g = row_group(sched, G, r, local);
-    if (g < 0) continue;
-    const int32_t* a_row = sched + (G + 1);
-    const TE* a = (g >= E) ? x + (size_t)(a_row[g] + local) * d : x_perm + (size_t)(a_row[g] + local) * d;
-    const TE* wgr = wg + ((size_t)g * F + f) * d;
-    const TE* wur = wu + ((size_t)g * F + f) * d;
+  const int64_t stride = (int64_t)gridDim.x * (blockDim.x / kQuad);
+  const int nv = d / 4;
+  // every lane runs the same number of iterations, so the quad's shuffles see all four lanes
+  for (int64_t o0 = (int64_t)blockIdx.x * (blockDim.x / kQuad); o0 < total; o0 += stride) {
+    const int64_t o = o0 + (threadIdx.x / kQuad);
     float sg = 0.f, su = 0.f;
-    for (int i = 0; i < d; ++i) {
-      const float av = to_f32(a[i]);
-      sg = fmaf(av, to_f32(wgr[i]), sg);
-      su = fmaf(av, to_f32(wur[i]), su);
+    int64_t r = 0;
+    int f = 0;
+    int g = -1;
+    if (o < total) {
+      r = o / F;
+      f = (int)(o % F);
+      int local = 0;
+      g = row_group(sched, G, r, local);
+      if (g >= 0) {
+        const int32_t* a_row = sched + (G + 1);
+        const float4* a = reinterpret_cast<const float4*>((g >= E) ? x + (size_t)(a_row[g] + local) * d
+                                                                   : x_perm + (size_t)(a_row[g] + local) * d);
+        const float4* wgr = reinterpret_cast<const float4*>(wg + ((size_t)g * F + f) * d);
+        const float4* wur = reinterpret_cast<const float4*>(wu + ((size_t)g * F + f) * d);
+        for (int v = p; v < nv; v += kQuad) {
+          const float4 av = __ldg(a + v), gv = __ldg(wgr + v), uv = __ldg(wur + v);
+          sg = fmaf(av.x, gv.x, sg); sg = fmaf(av.y, gv.y, sg); sg = fmaf(av.z, gv.z, sg); sg = fmaf(av.w, gv.w, sg);
+          su = fmaf(av.x, uv.x, su); su = fmaf(av.y, uv.y, su); su = fmaf(av.z, uv.z, su); su = fmaf(av.w, uv.w, su);
+        }
+      }
     }
-    h[(size_t)r * F + f] = from_f32<TE>(silu_precise(sg) * su);
+    sg = quad_sum(sg);
+    su = quad_sum(su);
+    if (o < total && g >= 0 && p == 0) h[(size_t)r * F + f] = silu_precise(sg) * su;
   }
 }
 
-template <typename TE>
-__global__ void ffn_down_fma_kernel(const TE* __restrict__ h, const TE* __restrict__ wd,
+__global__ void ffn_down_fma_kernel(const float* __restrict__ h, const float* __restrict__ wd,
                                     const int32_t* __restrict__ sched, int G, int d, int F, int64_t n_rows,
-                                    TE* __restrict__ y) {
+                                    float* __restrict__ y) {
+  const int p = threadIdx.x & (kQuad - 1);
   const int64_t total = n_rows * d;
-  for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = o / d;
-    const int c = (int)(o % d);
-    int local = 0;
-    const int g = row_group(sched, G, r, local);
-    if (g < 0) continue;
-    const TE* hr = h + (size_t)r * F;
-    const TE* wr = wd + ((size_t)g * d + c) * F;
+  const int64_t stride = (int64_t)gridDim.x * (blockDim.x / kQuad);
+  const int nv = F / 4;
+  for (int64_t o0 = (int64_t)blockIdx.x * (blockDim.x / kQuad); o0 < total; o0 += stride) {
+    const int64_t o = o0 + (threadIdx.x / kQuad);
     float acc = 0.f;
-    for (int f = 0; f < F; ++f) acc = fmaf(to_f32(hr[f]), to_f32(wr[f]), acc);
-    y[(size_t)r * d + c] = from_f32<TE>(acc);
+    int64_t r = 0;
+    int c = 0;
+    int g = -1;
+    if (o < total) {
+      r = o / d;
+      c = (int)(o % d);
+      int local = 0;
+      g = row_group(sched, G, r, local);
+      if (g >= 0) {
+        const float4* hr = reinterpret_cast<const float4*>(h + (size_t)r * F);
+        const float4* wr = reinterpret_cast<const float4*>(wd + ((size_t)g * d + c) * F);
+        for (int v = p; v < nv; v += kQuad) {
+          const float4 hv = __ldg(hr + v), wv = __ldg(wr + v);
+          acc = fmaf(hv.x, wv.x, acc); acc = fmaf(hv.y, wv.y, acc); acc = fmaf(hv.z, wv.z, acc);
+          acc = fmaf(hv.w, wv.w, acc);
+        }
+      }
+    }
+    acc = quad_sum(acc);
+    if (o < total && g >= 0 && p == 0) y[(size_t)r * d + c] = acc;
   }
 }
 
@@ -109,21 +148,22 @@ cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, co
                            const void* w_down, const void* sched, void* h, void* y, cudaStream_t st,
                            cudaEvent_t mid_event) {
   const int64_t n_rows = s.R + (int64_t)s.S * s.T;
-  const int threads = 256;
+  const int threads = 256;                      // 64 output elements per block (four lanes each)
+  const int64_t per_block = threads / 4;
   const int64_t cap = (int64_t)num_sms() * 32;
-  int64_t b1 = (n_rows * s.F + threads - 1) / threads;
-  int64_t b2 = (n_rows * s.d + threads - 1) / threads;
+  int64_t b1 = (n_rows * s.F + per_block - 1) / per_block;
+  int64_t b2 = (n_rows * s.d + per_block - 1) / per_block;
   b1 = b1 < cap ? (b1 < 1 ? 1 : b1) : cap;
   b2 = b2 < cap ? (b2 < 1 ? 1 : b2) : cap;
   const int32_t* sc = static_cast<const int32_t*>(sched);
   // float32 layers only; bf16 layers run on the tensor cores
-  ffn_gateup_fma_kernel<float><<<(unsigned)b1, threads, 0, st>>>(
+  ffn_gateup_fma_kernel<<<(unsigned)b1, threads, 0, st>>>(
       static_cast<const float*>(x_perm), static_cast<const float*>(x), static_cast<const float*>(w_gate),
       static_cast<const float*>(w_up), sc, s.G, s.E, s.d, s.F, n_rows, static_cast<float*>(h));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
-  ffn_down_fma_kernel<float><<<(unsigned)b2, threads, 0, st>>>(
+  ffn_down_fma_kernel<<<(unsigned)b2, threads, 0, st>>>(
       static_cast<const float*>(h), static_cast<const float*>(w_down), sc, s.G, s.d, s.F, n_rows,
       static_cast<float*>(y));
   return cudaGetLastError();

@@ -36,6 +36,7 @@ struct WsLayout {
   size_t xq_scale;      // [T] float: W8A8 per-token scales (the per-token codes use the x_perm region)
   size_t h8;            // [(R+S*T)*F] bytes: W8A8 E4M3 codes of h
   size_t h8_scale;      // [R+S*T] float: their per-row scales
+  size_t mlp_ready;     // [m-tiles] int32: the one-launch expert MLP's per-m-tile h counters
   size_t total;
 };
 
@@ -143,6 +144,14 @@ cudaError_t launch_gemm_gateup_fp8w(const Shape& s, const void* x_perm, const vo
                                     void* h, int32_t* status, cudaStream_t st);
 cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* wd_q, const float* wd_s,
                                   const void* sched, void* y, int32_t* status, cudaStream_t st);
+
+// Both contractions of the bf16 expert MLP in one persistent launch (gemm_fused.cu); `ready`
+// holds fused_mlp_ready_ints(s) int32 (zeroed by the launcher).
+bool fused_mlp_supported(const Shape& s);
+int64_t fused_mlp_ready_ints(const Shape& s);
+cudaError_t launch_mlp_fused_tc(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
+                                const void* w_up, const void* w_down, const void* sched, void* h, void* y,
+                                int32_t* ready, int32_t* status, cudaStream_t st);
 
 // W8A8 (E4M3 weights and activations, gemm_w8a8.cu).
 bool w8a8_supported(const Shape& s);

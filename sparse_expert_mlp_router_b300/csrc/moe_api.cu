@@ -130,6 +130,7 @@ WsLayout make_layout(const Shape& s) {
     L.xq_scale = take((size_t)s.T * 4);
     L.h8 = take(grouped * s.F);
     L.h8_scale = take(grouped * 4);
+    L.mlp_ready = take((size_t)fused_mlp_ready_ints(s) * 4);
   }
   L.total = o;
   return L;
@@ -203,6 +204,19 @@ cudaError_t run_schedule(const Shape& s, const WsLayout& L, void* ws, const int3
   return launch_group_schedule(s, offsets, at<void>(ws, L.sched), at<int32_t>(ws, L.status), st);
 }
 
+// Whether the bf16 expert MLP runs as one persistent launch of both contractions instead of
+// two launches: by default for batches of one 128-token chunk (decode), where the down tiles of
+// the first experts fill the gate/up launch's last round of tiles and the gap between the
+// launches (decode layer 0.192 -> 0.187 ms); on the prefill layers, which run at the power
+// limit, it measured the same as two launches. MOE_FUSED_MLP=1 / 0 in the environment (read
+// at every call) forces it on / off.
+bool fused_mlp(const Shape& s) {
+  if (!fused_mlp_supported(s)) return false;
+  const char* v = getenv("MOE_FUSED_MLP");
+  if (v != nullptr && (v[0] == '0' || v[0] == '1')) return v[0] == '1';
+  return s.nchunks == 1;
+}
+
 // Expert weights of a call: bf16 / float32 tensors, or FP8 codes with per-row scales.
 struct ExpertWeights {
   const void* g;
@@ -227,6 +241,11 @@ cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_p
       return e;
     if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
     return launch_gemm_down_fp8w(s, h, static_cast<const uint8_t*>(w.d), w.ds, sched, y, status, st);
+  }
+  if (s.dtype == MOE_BF16 && fused_mlp(s)) {
+    // one launch for both contractions: the stage boundary event falls before it
+    if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
+    return launch_mlp_fused_tc(s, x_perm, x, w.g, w.u, w.d, sched, h, y, at<int32_t>(ws, L.mlp_ready), status, st);
   }
   if (s.dtype == MOE_BF16) {
     if ((e = launch_gemm_gateup_tc(s, x_perm, x, w.g, w.u, sched, h, status, st)) != cudaSuccess) return e;
@@ -263,7 +282,8 @@ bool fused_combine(const Shape& s, const ExpertWeights& w) {
 int layer_launches(const Shape& s) {
   // hist, scan (+ group schedule), scatter, gather; one CTA for the first three when the batch
   // is a single chunk of tokens
-  const int router = 1, grouping = s.nchunks == 1 ? 2 : 4, mlp = 2, combine = 1;
+  const int router = 1, grouping = s.nchunks == 1 ? 2 : 4, mlp = (s.dtype == MOE_BF16 && fused_mlp(s)) ? 1 : 2,
+            combine = 1;
   return router + grouping + mlp + combine;
 }
 
@@ -562,6 +582,12 @@ moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, con
 int32_t moe_layer_launch_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return -1;
   return layer_launches(make_shape(*cfg));
+}
+
+int32_t moe_layer_mlp_fused(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return -1;
+  const Shape s = make_shape(*cfg);
+  return (s.dtype == MOE_BF16 && fused_mlp(s)) ? 1 : 0;
 }
 
 moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns, cudaStream_t stream) {

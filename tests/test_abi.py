@@ -143,9 +143,21 @@ def test_fp8_quantiser_and_stats_validation_before_any_launch():
     assert L.moe_routing_stats(ctypes.byref(_cfg(top_k=300)), p, p, None) == moe.MOE_ERR_INVALID_ARG
 
 
-def test_launch_count_follows_the_grouping_path():
+def test_launch_count_follows_the_grouping_path(monkeypatch):
     # router, grouping (one kernel for a single 128-token chunk, else histogram, scan and
-    # scatter), the row copy, the two grouped GEMMs and the combine
-    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 2 + 1
+    # scatter), the row copy, the expert MLP (one persistent launch of both contractions for a
+    # single chunk of a bf16 layer, else two) and the combine
+    monkeypatch.delenv("MOE_FUSED_MLP", raising=False)
+    assert moe.moe_layer_mlp_fused(_cfg(T=128)) == 1
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 1 + 1
+    assert moe.moe_layer_mlp_fused(_cfg(T=129)) == 0
     assert moe.moe_layer_launch_count(_cfg(T=129)) == 1 + 4 + 2 + 1
     assert moe.moe_layer_launch_count(_cfg(top_k=300)) == -1
+    assert moe.moe_layer_mlp_fused(_cfg(top_k=300)) == -1
+    # the environment forces either way (read at every call); float32 layers always take two
+    monkeypatch.setenv("MOE_FUSED_MLP", "0")
+    assert moe.moe_layer_mlp_fused(_cfg(T=128)) == 0
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 2 + 1
+    monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    assert moe.moe_layer_mlp_fused(_cfg(T=129)) == 1
+    assert moe.moe_layer_mlp_fused(_cfg(T=128, dtype="f32")) == 0

@@ -142,3 +142,17 @@ def test_w8a8_layer_writes_only_its_outputs(name, edit):
                                bufs["out"].t, bufs["workspace"].t)
     assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
     _check_all(bufs, f"w8a8 layer {name}")
+
+
+@pytest.mark.parametrize("name,edit", [("mini_deepseek", {}), ("mini_decode", {}), ("mini_mixtral", {"T": 1200})])
+def test_fused_mlp_layer_writes_only_its_outputs(name, edit, monkeypatch):
+    # the one-launch expert MLP keeps its per-m-tile counters inside the workspace
+    monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    w = synth.WORKLOADS[name].with_(**edit)
+    dev = Inputs(w).device()
+    cfg = cfg_of(w)
+    bufs = {"out": Guarded((w.T, w.d_model), torch.bfloat16), "workspace": _workspace(cfg)}
+    moe.moe_layer_forward(cfg, dev["x"], dev["w_router"], dev["bias"], dev["w_gate"], dev["w_up"], dev["w_down"],
+                          bufs["out"].t, bufs["workspace"].t)
+    assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
+    _check_all(bufs, f"fused mlp layer {name}")

@@ -205,3 +205,50 @@ def test_layer_fused_combine_full_size_qwen3(monkeypatch):
     assert_close(to_f64(out), to_f64(ref_out), 1e-2, "fused vs separate combine")
     del dev
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------- both contractions in one persistent launch
+
+@pytest.mark.parametrize("name,edit", [
+    ("mini_mixtral", {}),
+    ("mini_qwen3", {}),
+    ("mini_deepseek", {}),                                         # drops, shared expert
+    ("mini_decode", {}),
+    ("mini_mixtral", dict(T=1)),
+    ("mini_qwen3", dict(bias_s=8.0, top_k=2)),                     # mostly empty experts
+    ("mini_mixtral", dict(T=1200)),                                # ten-tile experts
+    ("mini_deepseek", dict(capacity_factor=0.05)),
+])
+def test_layer_fused_mlp_is_bit_identical(name, edit, monkeypatch):
+    # MOE_FUSED_MLP=1: the gate/up and down tiles in one launch, down tiles of an m-tile started
+    # once its h rows are published (the default for single-chunk batches); =0: two launches.
+    # Same tiles, same arithmetic: the outputs agree bit for bit, and with the oracle within
+    # the usual tolerance
+    w = synth.WORKLOADS[name].with_(**edit)
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    monkeypatch.setenv("MOE_FUSED_MLP", "0")                      # two launches
+    ref_out, ref_idx, _ = _run_layer(w, dev, cfg)
+    monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    out, idx, counts = _run_layer(w, dev, cfg)
+    assert (idx == ref_idx).all()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    res, _ = _oracle_on_gpu_routing(w, inp.f64["x"], inp.f64["w_router"], inp.bias, inp.expert, idx)
+    assert_close(to_f64(out), res.out, out_tolerance(w), f"fused mlp {name} {edit}")
+
+
+@pytest.mark.parametrize("name", ["mixtral_8x7b", "qwen3_30b_a3b", "deepseek_v3", "decode_qwen3"])
+def test_layer_fused_mlp_full_size_bit_identical(name, monkeypatch):
+    w = synth.WORKLOADS[name]
+    cfg = cfg_of(w)
+    dev = synth.device_inputs(w)
+    monkeypatch.setenv("MOE_FUSED_MLP", "0")                      # two launches
+    ref_out, ref_idx, _ = _run_layer(w, dev, cfg)
+    monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    for _ in range(2):                                             # twice: the counters restart
+        out, idx, _ = _run_layer(w, dev, cfg)
+        assert (idx == ref_idx).all()
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    del dev
+    torch.cuda.empty_cache()
