@@ -16,7 +16,7 @@ value        tokens/s with inputs resident in HBM: K steps timed with CUDA event
              (barrier + synchronize on both sides, max over ranks); the expert
              weights exceed the 126 MB L2, so every step streams them from HBM.
              The K moe_layer_forward calls run as one CUDA-graph replay; about one
-             layer in 25 (at least four) carries CUDA events at the stage boundaries,
+             layer in 25 (at least two) carries CUDA events at the stage boundaries,
              so the stage times come from the timed replay itself, under the same
              clocks and power. --eager: K separate calls with the stage events.
 e2e          the same metric through the same C-ABI call with the activations in
@@ -487,8 +487,8 @@ def run_reference(args, w):
 
 def staged_positions(K: int) -> list:
     """Which of the K timed layers carry the stage events: about one in 25 (at least
-    min(K, 4) of them), evenly spread, the last one included."""
-    n = min(K, max(4, K // 25))
+    min(K, 2) of them), evenly spread, the last one included."""
+    n = min(K, max(2, K // 25))
     return [((j + 1) * K) // n - 1 for j in range(n)]
 
 

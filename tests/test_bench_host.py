@@ -106,7 +106,7 @@ def test_source_hash_ignores_comments_but_not_code():
 def test_stage_event_layers_are_spread_over_the_timed_replay():
     for K in (1, 3, 4, 20, 100, 500, 1001):
         pos = bench.staged_positions(K)
-        assert len(pos) == min(K, max(4, K // 25))
+        assert len(pos) == min(K, max(2, K // 25))
         assert pos == sorted(set(pos)) and pos[-1] == K - 1 and pos[0] >= 0
         gaps = [b - a for a, b in zip([-1] + pos, pos)]
         assert max(gaps) - min(gaps) <= 1                 # evenly spread
