@@ -70,6 +70,7 @@ CPU_MIN_S = 0.5                      # CPU baseline: repeat a small sample to at
 CPU_MAX_REPS = 200
 # float32 FMA rate of the CUDA cores: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
 F32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+NOMINAL_HBM_GBS = 8000.0             # HBM3e's nominal ~8 TB/s (the measured copy bandwidth is the roofline)
 
 
 def parse_args(argv=None):
@@ -151,6 +152,20 @@ def algorithmic(w, kept_pairs: int, groups_touched: int, weight_bytes: float = 2
         "down_bytes": dn_w + rows * F * e + rows * d * e,
         "weight_bytes": gu_w + dn_w,
     }
+
+
+def layer_totals(w, kept_pairs: int, groups_touched: int, weight_bytes: float = 2.0) -> dict:
+    """Flops and HBM bytes of one whole layer forward with its intermediate round trips: the
+    expert MLPs and the router; the touched experts' weights, x in, the grouped x rows written
+    and read, h written and read, the grouped outputs written and read, and the output."""
+    rows = kept_pairs + w.n_shared * w.T
+    d, F = w.d_model, w.d_ff
+    e = 2 if w.dtype == "bf16" else 4
+    flops = 6.0 * d * F * rows + 2.0 * w.T * d * w.n_experts
+    weights = groups_touched * 3.0 * d * F * weight_bytes
+    bytes_ = (weights + w.T * d * e + kept_pairs * d * e * 2 + rows * F * e * 2 + rows * d * e * 2
+              + w.T * d * e)
+    return {"flops": flops, "bytes": bytes_}
 
 
 class ClockSampler:
@@ -735,6 +750,7 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
                          [float(v) for v in stage.mean(axis=0)]))
     pair_flops = work["gateup_flops"] + work["down_flops"]
+    layer_work = layer_totals(w, kept, touched, 1.0 if fp8 else (2.0 if w.dtype == "bf16" else 4.0))
     weight_bytes = work["weight_bytes"]
     res = {
         "value": value, "ms_per_step": max_ms / K, "steps": K,
@@ -752,6 +768,13 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
         "grouped_gemm_frac_of_burst": pair_flops / (pair_ms / 1e3) / 1e12 / (peaks["bf16_tflops"] * tensor_mult),
         "expert_weight_gbs": weight_bytes / (pair_ms / 1e3) / 1e9,
         "expert_weight_frac_of_hbm": weight_bytes / (pair_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+        "grouped_gemm_frac_of_sustained": pair_flops / (pair_ms / 1e3) / 1e12 / (peaks["bf16_tflops_sustained"]
+                                                                                  * tensor_mult),
+        "expert_weight_frac_of_nominal_hbm": weight_bytes / (pair_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        # the whole layer against its own roofline: the longer of (all flops / tensor rate) and
+        # (all bytes / HBM bandwidth), over the layer time
+        "layer_roofline_frac": max(layer_work["flops"] / (peaks["bf16_tflops"] * tensor_mult * 1e12),
+                                   layer_work["bytes"] / (peaks["hbm_gbs"] * 1e9)) / (max_ms / K / 1e3),
     }
     del dev, ws, out, counts, wargs, args_fwd
     torch.cuda.synchronize()

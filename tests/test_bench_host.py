@@ -110,3 +110,12 @@ def test_stage_event_layers_are_spread_over_the_timed_replay():
         assert pos == sorted(set(pos)) and pos[-1] == K - 1 and pos[0] >= 0
         gaps = [b - a for a, b in zip([-1] + pos, pos)]
         assert max(gaps) - min(gaps) <= 1                 # evenly spread
+
+
+def test_layer_totals_count_every_round_trip():
+    w = synth.Workload("hand", T=4, d_model=8, n_experts=2, top_k=1, d_ff=16, n_shared=1)
+    t = bench.layer_totals(w, kept_pairs=4, groups_touched=3)
+    rows = 4 + 4
+    assert t["flops"] == 6 * 8 * 16 * rows + 2 * 4 * 8 * 2
+    # weights, x, x_perm (write + read), h (write + read), y_perm (write + read), out
+    assert t["bytes"] == 3 * 3 * 8 * 16 * 2 + 4 * 8 * 2 + 4 * 8 * 2 * 2 + rows * 16 * 2 * 2 + rows * 8 * 2 * 2 + 4 * 8 * 2

@@ -4,7 +4,8 @@ Each case draws tokens, widths, experts, top-k, shared expert, score function, g
 renormalisation, capacity and router-bias skew from a fixed seed (so the case list is the same
 on every run), runs moe_layer_forward, and compares routing, counts and every output element
 with the oracle re-run on the GPU's routing. bf16 cases whose shapes the FP8 kernels take are
-also run with FP8 weights against the oracle on the dequantized weights.
+also run with FP8 weights against the oracle on the dequantized weights, and with FP8 weights
+and activations (W8A8) against the oracle's W8A8 reading.
 """
 import numpy as np
 import pytest
@@ -87,3 +88,16 @@ def test_layer_sweep(w):
     experts8 = lambda g: (q["w_gate"][2][g], q["w_up"][2][g], q["w_down"][2][g])
     res8 = _oracle_on_gpu_routing(w, inp, experts8, gidx)
     assert_close(to_f64(out8), res8.out, out_tolerance(w), w.name + " fp8")
+
+    # and with E4M3 activations as well (W8A8), against the oracle's W8A8 reading
+    outa = torch.full_like(out, float("nan"))
+    moe.moe_layer_forward_w8a8(cfg, dev["x"], dev["w_router"], dev["bias"], q["w_gate"][0], q["w_gate"][1],
+                               q["w_up"][0], q["w_up"][1], q["w_down"][0], q["w_down"][1], outa, ws)
+    assert moe.moe_get_device_error(ws) == moe.MOE_OK
+    resa = O.layer_forward(inp.f64["x"], inp.f64["w_router"], inp.bias, experts8, top_k=w.top_k, score=w.score,
+                           renormalize=w.renormalize, capacity_factor=w.capacity_factor, n_shared=w.n_shared,
+                           mlp=O.expert_mlp_w8a8,
+                           routing=(gidx, oracle_gates_for(gidx, O.scores_from_logits(
+                               O.router_logits(inp.f64["x"], inp.f64["w_router"], inp.bias), w.score),
+                               w.renormalize)))
+    assert_close(to_f64(outa), resa.out, out_tolerance(w), w.name + " w8a8")
