@@ -92,7 +92,7 @@ def parse_args(argv=None):
     ap.add_argument("--weights", choices=["bf16", "fp8", "w8a8"], default="bf16",
                     help="expert weights as stored: bf16, or FP8 E4M3 codes with per-row scales (fp8), or "
                          "those weights with the expert inputs quantised to E4M3 per row as well (w8a8)")
-    ap.add_argument("--traffic-kind", choices=["bf16", "fp8", "w8a8", "fused"], default=None,
+    ap.add_argument("--traffic-kind", choices=["bf16", "fp8", "w8a8", "fused", "w8a8_fused"], default=None,
                     help="with --write-traffic: which kernels the CSVs hold (default: --weights)")
     ap.add_argument("--write-traffic", metavar="CSV_DIR", default=None,
                     help="write profiles/traffic.json from ncu CSVs traffic_<workload>.csv in CSV_DIR (see "
@@ -227,10 +227,11 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
-GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "gemm_common.cuh", "tc_ptx.cuh"),
+GEMM_SOURCES = {"bf16": ("gemm_tc.cu", "epilogue.cuh", "gemm_common.cuh", "tc_ptx.cuh"),
                 "fused": ("gemm_fused.cu", "epilogue.cuh", "gemm_common.cuh", "tc_ptx.cuh"),
                 "fp8": ("gemm_fp8w.cu", "gemm_common.cuh", "tc_ptx.cuh"),
-                "w8a8": ("gemm_w8a8.cu", "fp8_quant.cuh", "gemm_common.cuh", "tc_ptx.cuh")}
+                "w8a8": ("gemm_w8a8.cu", "epilogue.cuh", "fp8_quant.cuh", "gemm_common.cuh", "tc_ptx.cuh"),
+                "w8a8_fused": ("gemm_w8a8_fused.cu", "epilogue.cuh", "fp8_quant.cuh", "gemm_common.cuh", "tc_ptx.cuh")}
 
 
 def code_only(src: str) -> str:
@@ -295,7 +296,7 @@ def write_traffic(csv_dir: str, weights: str) -> None:
                     "bytes_per_launch": gu["dram__bytes_read.sum"] + gu["dram__bytes_write.sum"],
                     "read": gu["dram__bytes_read.sum"], "write": gu["dram__bytes_write.sum"],
                     "ns_under_ncu": gu["gpu__time_duration.sum"]}
-        if weights != "fused":                      # the one-launch MLP has no separate down kernel
+        if weights not in ("fused", "w8a8_fused"):  # the one-launch MLP has no separate down kernel
             dn = list(per.values())[1]
             out[key]["down_bytes_per_launch"] = dn["dram__bytes_read.sum"] + dn["dram__bytes_write.sum"]
     out["_comment"] = ("DRAM bytes per launch of the gate/up grouped GEMM (and of the down GEMM) from one-pass ncu "
@@ -708,7 +709,8 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
     # the bf16 layer's expert MLP may run as one launch of both contractions (decode-shaped
     # batches): then the dominant kernel is that launch, timed over both stages, with the flops
     # and bytes of both contractions
-    one_mlp = (not fp8) and w.dtype == "bf16" and moe.moe_layer_mlp_fused(cfg) == 1
+    one_mlp = (w.dtype == "bf16" and
+               moe.moe_layer_mlp_fused_weights(cfg, "w8a8" if a8 else "fp8" if fp8 else "bf16") == 1)
     peaks, peak_src = load_peaks()
     # the E4M3 x E4M3 tensor-core rate is twice the bf16 one (nominal dense 4.5 vs 2.25 PFLOP/s):
     # W8A8 contractions are compared with twice the measured bf16 rate
@@ -734,7 +736,9 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
         else:
             achieved = r_bytes / (gemm_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-        roof["kernel"] = ("grouped_mlp_fused_kernel<gate/up + SwiGLU, then down, one launch> (tcgen05)" if one_mlp else
+        roof["kernel"] = ("grouped_mlp_w8a8_fused_kernel<gate/up + SwiGLU, h to E4M3, then down, one launch> "
+                          "(tcgen05 kind::f8f6f4)" if one_mlp and a8 else
+                          "grouped_mlp_fused_kernel<gate/up + SwiGLU, then down, one launch> (tcgen05)" if one_mlp else
                           "grouped_gemm_w8a8_kernel<gate/up, E4M3 weights and activations, SwiGLU epilogue> "
                           "(tcgen05 kind::f8f6f4)" if a8 else
                           "grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else
@@ -743,9 +747,22 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
                                (("2 x " if a8 else "") + f"{peak_src} bf16 ") +
                                (f"sustained (timed region {max_ms / 1e3:.1f} s)" if long_run else "burst"))
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = (measured_traffic(w.name, "fused" if one_mlp else "w8a8" if a8 else "fp8" if fp8 else "bf16")
+    roof["traffic"] = (measured_traffic(w.name, ("w8a8_fused" if a8 else "fused") if one_mlp else
+                                        "w8a8" if a8 else "fp8" if fp8 else "bf16")
                        if w.dtype == "bf16" else None)
     roof["ms_per_launch"] = gemm_ms
+    # decode-shaped batches: the router prefetched the first experts' W_gate / W_up into L2, so
+    # that many of the kernel's algorithmic bytes came from L2 (read from HBM during routing);
+    # the kernel's rate without them is reported beside it, the whole layer's in layer_roofline_frac
+    warm = moe.moe_layer_l2_warm_bytes(cfg, weights if fp8 else "bf16") if w.dtype == "bf16" else 0
+    roof["l2_warm_bytes"] = warm
+    if warm > 0 and roof["bound"] == "hbm":
+        # W_gate + W_up of experts 0 .. n-1; those of the experts the batch touched are in r_bytes
+        per_expert = 2.0 * w.d_ff * w.d_model * (1.0 if fp8 else 2.0)
+        n_warm = int(round(warm / per_expert))
+        used = float((np.minimum(c, cap)[:n_warm] > 0).sum()) * per_expert
+        roof["l2_warm_bytes_touched"] = used
+        roof["frac_without_warm_bytes"] = (r_bytes - used) / (gemm_ms / 1e3) / 1e9 / roof["peak"]
 
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
                          [float(v) for v in stage.mean(axis=0)]))
@@ -756,10 +773,7 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
         "value": value, "ms_per_step": max_ms / K, "steps": K,
         "config": config_of(w, kept, touched, world, weights if fp8 else "bf16"),
         "e2e": e2e,
-        # moe_layer_launch_count counts the bf16 layer; the FP8 layers run the expert MLP as two
-        # launches, and W8A8 adds the quantiser of h
-        "gpu_launches": K * (moe.moe_layer_launch_count(cfg) + (moe.moe_layer_mlp_fused(cfg) if fp8 else 0)
-                             + (1 if a8 else 0)),
+        "gpu_launches": K * moe.moe_layer_launch_count_weights(cfg, weights if fp8 else "bf16"),
         "roofline": roof,
         "clocks": clocks,
         "stages_ms": stages_ms,

@@ -326,23 +326,52 @@ moe_status_t moe_layer_forward_w8a8_timed(const moe_config_t* cfg, const void* x
                                           void* const* events, int32_t n_events, cudaStream_t stream);
 
 /* Number of kernel launches one moe_layer_forward call (bf16 or float32 weights) enqueues for this
- * configuration (-1 if invalid). The FP8-weight layer launches two expert-MLP kernels where
- * moe_layer_mlp_fused reports one, and the W8A8 layer one more (the quantiser of h). */
+ * configuration (-1 if invalid). Memset nodes are not counted. */
 int32_t moe_layer_launch_count(const moe_config_t* cfg);
 
+/* The same for the layer call with the given weights: 0 bf16 / float32 (moe_layer_forward),
+ * 1 FP8 codes with bf16 activations (moe_layer_forward_fp8), 2 W8A8 (moe_layer_forward_w8a8);
+ * -1 if the configuration is invalid or the FP8 kernels do not take it. */
+int32_t moe_layer_launch_count_weights(const moe_config_t* cfg, int32_t weights);
+
 /*
- * 1 if moe_layer_forward runs the expert MLP's two contractions (gate/up + SwiGLU, then down)
- * as one persistent launch for this configuration, 0 if as two, -1 if the configuration is
- * invalid. One launch is the default for bf16 layers whose batch is a single chunk of at most
- * 128 tokens (decode): each CTA takes its gate/up tiles, then its down tiles, and a down tile
- * waits (bounded) until every gate/up tile of its 128-row block has published its rows of h
- * through a counter in the workspace. The results are bit-identical to the two launches.
+ * 1 if moe_layer_forward and moe_layer_forward_w8a8 run the expert MLP's two contractions
+ * (gate/up + SwiGLU, then down; in W8A8 with h's quantisation between them) as one persistent
+ * launch for this configuration, 0 if as separate launches, -1 if the configuration is invalid.
+ * One launch is the default for bf16 layers whose batch is a single chunk of at most 128 tokens
+ * (decode): each CTA takes its gate/up tiles, then its down tiles, and a down tile waits
+ * (bounded) until every gate/up tile of its 128-row block has published its rows of h through a
+ * counter in the workspace (in W8A8 the tile that completes a block quantises its rows first).
+ * The results are bit-identical to the separate launches.
  * MOE_FUSED_MLP=1 or 0 in the environment forces one or two launches for every bf16 layer
  * whose d_model is a multiple of 256 (read at every call). The one launch needs all of its
  * CTAs (one per SM) resident at once: a GPU shared with other work that holds SMs for long can
  * make its waits run out (MOE_ERR_TIMEOUT in the status word) instead of hanging.
  */
 int32_t moe_layer_mlp_fused(const moe_config_t* cfg);
+
+/*
+ * moe_layer_mlp_fused per weight format (`weights` as in moe_layer_launch_count_weights): 1 if
+ * the expert MLP runs as one launch, 0 if not, -1 for an invalid config or a format the shape
+ * does not take. FP8 weights with bf16 activations: always two launches. W8A8: one launch (the
+ * tile that completes an m-tile's gate/up quantises its h rows, then its down tiles start) only
+ * with MOE_FUSED_MLP=1, since it measured slower than gate/up, quantiser and down as three
+ * launches.
+ */
+int32_t moe_layer_mlp_fused_weights(const moe_config_t* cfg, int32_t weights);
+
+/*
+ * Bytes of expert weights the whole-layer call on `cfg` prefetches into L2 while its router
+ * runs (0 if none), with `weights` as in moe_layer_launch_count_weights; -1 for an invalid
+ * config or a weights mode the shape does not take. A batch of at most 128 tokens (decode)
+ * leaves HBM idle during routing and grouping, after which the expert MLP streams the touched
+ * experts' weights, its first tiles the gate/up rows of the lowest-index experts; so the
+ * router prefetches W_gate and W_up of experts 0 .. n-1, as many as fit the budget
+ * (MOE_L2_WARM_MB in the environment, read at every call, 0 = off; default 64 MB). A hint
+ * only: results do not depend on it. Mixture-of-Experts pages, "Memory vs compute,
+ * quantified" (decode reads each touched expert's weights once).
+ */
+int64_t moe_layer_l2_warm_bytes(const moe_config_t* cfg, int32_t weights);
 
 /*
  * Synchronise `stream`, then return the first device-side status recorded in the workspace

@@ -11,13 +11,24 @@
 
 namespace moe {
 
+// 16 bytes of a row: through the read-only cache path when the row was written before the
+// launch, or from L2 (__ldcg) when other SMs of the same launch may have just written it (the
+// read-only path is not kept coherent with such writes).
+template <bool FROM_L2>
+__device__ __forceinline__ uint4 load_row16(const __nv_bfloat16* p) {
+  if (FROM_L2) return __ldcg(reinterpret_cast<const uint4*>(p));
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
 // Row `src` of `cols` bf16 values (cols a multiple of 16, rows 16-byte aligned) -> `dst`
 // codes and *scale_out (written by lane 0). All 32 lanes of the warp call it together.
-__device__ __forceinline__ void quantize_row_e4m3_warp(const __nv_bfloat16* __restrict__ src, int cols,
-                                                       uint8_t* __restrict__ dst, float* scale_out, int lane) {
+// FROM_L2: the row may have been written by other SMs during the same launch.
+template <bool FROM_L2 = false>
+__device__ __forceinline__ void quantize_row_e4m3_warp(const __nv_bfloat16* src, int cols, uint8_t* __restrict__ dst,
+                                                       float* scale_out, int lane) {
   float mx = 0.0f;
   for (int c = lane * 8; c < cols; c += 256) {
-    const uint4 u = *reinterpret_cast<const uint4*>(src + c);
+    const uint4 u = load_row16<FROM_L2>(src + c);
     const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -30,8 +41,8 @@ __device__ __forceinline__ void quantize_row_e4m3_warp(const __nv_bfloat16* __re
   const float s = __fdiv_rn(mx, 448.0f);
   if (lane == 0) *scale_out = s;
   for (int c = lane * 16; c < cols; c += 512) {
-    const uint4 a = *reinterpret_cast<const uint4*>(src + c);
-    const uint4 b = *reinterpret_cast<const uint4*>(src + c + 8);
+    const uint4 a = load_row16<FROM_L2>(src + c);
+    const uint4 b = load_row16<FROM_L2>(src + c + 8);
     const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t out[4];
 #pragma unroll

@@ -58,6 +58,7 @@
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
 #include "gemm_common.cuh"
+#include "epilogue.cuh"
 
 namespace moe {
 namespace {
@@ -93,69 +94,9 @@ struct GemmArgs {
   int routed_groups;          // E: groups >= E are the shared expert (weight one, row = token)
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
-
-constexpr int kStageOutBytes = 32 * 64;   // one epilogue warp's staging: 32 rows x 32 bf16
-
-// Epilogue of one warp's 32 accumulator rows (TMEM lanes; this thread holds row `lane`):
-// output columns [half * COLS/2, (half + 1) * COLS/2) of the tile, rows 0 .. nvalid-1 written
-// at orow0 + r * ldo. MODE 0 reads gate columns [0,128) and up columns [128,256) of the
-// accumulator and writes COLS = 128 columns of silu(gate) * up.
-// Each 32-column chunk is converted to bf16 in registers (one 64-byte row piece per thread),
-// staged in the warp's 2 KB of shared memory, and read back so that each store instruction
-// writes 8 rows x 64 contiguous bytes (whole 32-byte sectors) instead of 32 rows x 16 bytes.
-// In the staging buffer, row r's 16-byte piece j sits at r * 64 + 16 * (j ^ ((r >> 1) & 3)),
-// which keeps both the row-wise writes and the column-wise reads free of bank conflicts.
-template <int MODE, int COLS>
-__device__ __forceinline__ void store_tile(uint32_t t_row, int nvalid, __nv_bfloat16* orow0, int64_t ldo, int half,
-                                           uint32_t stg, int lane) {
-  if (nvalid <= 0) return;                      // warp-uniform: no row of this warp is valid
-  const int c0 = half * (COLS / 2), c1 = c0 + COLS / 2;
-#pragma unroll 1
-  for (int c = c0; c < c1; c += 32) {
-    uint32_t packed[16];
-    if (MODE == 0) {
-      uint32_t gv[32], uv[32];
-      ptx::tmem_ld32(t_row + c, gv);
-      ptx::tmem_ld32(t_row + 128 + c, uv);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float h0 = silu_f(__uint_as_float(gv[2 * q])) * __uint_as_float(uv[2 * q]);
-        const float h1 = silu_f(__uint_as_float(gv[2 * q + 1])) * __uint_as_float(uv[2 * q + 1]);
-        packed[q] = pack_bf16(h0, h1);
-      }
-    } else {
-      uint32_t v[32];
-      ptx::tmem_ld32(t_row + c, v);
-      ptx::tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 16; ++q) packed[q] = pack_bf16(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
-    }
-    const uint32_t my_row = stg + (uint32_t)lane * 64u;
-    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      st_shared_v4(my_row + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-    __syncwarp();
-    const int j = lane & 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = 8 * q + (lane >> 2);
-      const uint4 v = ld_shared_v4(stg + (uint32_t)r * 64u + ((uint32_t)(j ^ ((r >> 1) & 3)) << 4));
-      if (r < nvalid) *reinterpret_cast<uint4*>(orow0 + (int64_t)r * ldo + c + 8 * j) = v;
-    }
-    __syncwarp();
-  }
-}
+using epi::kStageOutBytes;
+using epi::ld_shared_v4;
+using epi::st_shared_v4;
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -416,8 +357,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       } else {
         const int row0 = m * kBM + quarter * 32;                // the warp's first row in the group
         __nv_bfloat16* orow0 = args.out + ((int64_t)s_out_row[g] + row0) * args.ldo + (int64_t)n * C::kOutCols;
-        store_tile<MODE, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
-                                      stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
+        epi::store_tile<MODE == 0, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
+                                                stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty[acc]));
@@ -648,8 +589,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       const int row0 = m * kBM + quarter * 32;
       __nv_bfloat16* orow0 = args.out + ((int64_t)s_out_row[g] + row0) * args.ldo + (int64_t)n * C::kOutCols;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * C::kN);
-      store_tile<MODE, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
-                                    stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
+      epi::store_tile<MODE == 0, C::kOutCols>(t_row, s_rows[g] - row0, orow0, args.ldo, half,
+                                              stg_base + (uint32_t)(warp - 2) * kStageOutBytes, lane);
       ptx::tc_fence_before();
       ptx::mbar_arrive_cluster(tempty_leader + 8u * acc);
     }

@@ -23,6 +23,7 @@
 //               instruction
 // Tiles are ordered (group, n-tile, m-tile) over the schedule of the grouping stage. Every wait
 // is bounded (a stall records MOE_ERR_TIMEOUT, the roles leave, TMEM is freed).
+#include "epilogue.cuh"
 #include "fp8_quant.cuh"
 #include "gemm_common.cuh"
 #include "internal.cuh"
@@ -49,7 +50,7 @@ constexpr int kStageBytes = kABytes + kBBytes;    // 48 KB
 constexpr int kStages = 4;
 constexpr int kTmemCols = 512;                    // two accumulators of 256 columns
 constexpr int kSchedInts = 4 * (kMaxExperts + 2);
-constexpr int kStageOutBytes = 32 * 64;           // one epilogue warp's staging: 32 rows x 32 bf16
+using epi::kStageOutBytes;
 constexpr size_t kStgOff = (size_t)kStages * kStageBytes + 256 + (((size_t)kSchedInts * 4 + 127) / 128) * 128;
 constexpr size_t kSmem = 1024 + kStgOff + (size_t)kEpiWarps * kStageOutBytes;
 
@@ -71,16 +72,6 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
-
 struct W8Args {
   int K;                  // reduction length (codes)
   int n_tiles;            // N tiles per group
@@ -94,27 +85,6 @@ struct W8Args {
   int64_t ldo;
   int32_t* status;
 };
-
-// One warp's 32 rows of a 32-column chunk: this thread's row as 16 packed bf16 pairs, staged
-// and stored 8 rows x 64 contiguous bytes per instruction (row r's 16-byte piece j at
-// r * 64 + 16 * (j ^ ((r >> 1) & 3)) in the staging buffer), rows >= nvalid skipped.
-__device__ __forceinline__ void store_chunk(const uint32_t (&packed)[16], int nvalid, __nv_bfloat16* orow0,
-                                            int64_t ldo, int c, uint32_t stg, int lane) {
-  const uint32_t my_row = stg + (uint32_t)lane * 64u;
-  const uint32_t sw = (uint32_t)((lane >> 1) & 3);
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    st_shared_v4(my_row + ((j ^ sw) << 4), packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-  __syncwarp();
-  const int j = lane & 3;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int r = 8 * q + (lane >> 2);
-    const uint4 v = ld_shared_v4(stg + (uint32_t)r * 64u + ((uint32_t)(j ^ ((r >> 1) & 3)) << 4));
-    if (r < nvalid) *reinterpret_cast<uint4*>(orow0 + (int64_t)r * ldo + c + 8 * j) = v;
-  }
-  __syncwarp();
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -311,7 +281,7 @@ grouped_gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
               packed[q] = pack_bf16(__uint_as_float(v[2 * q]) * (sa * __ldg(sd + 2 * q)),
                                     __uint_as_float(v[2 * q + 1]) * (sa * __ldg(sd + 2 * q + 1)));
           }
-          store_chunk(packed, nvalid, orow0, args.ldo, c, stg, lane);
+          epi::store_chunk(packed, nvalid, orow0, args.ldo, c, stg, lane);
         }
       }
       ptx::tc_fence_before();

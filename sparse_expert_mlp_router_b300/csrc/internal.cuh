@@ -27,16 +27,16 @@ struct WsLayout {
   size_t sched;         // [4*(G+1)] int32: group schedule of the grouped GEMMs
   size_t dest_row;      // [T*k] int32
   size_t src_token;     // [R] int32
-  size_t x_perm;        // [R*d] elements (at least T*d bytes: the W8A8 per-token codes)
+  size_t x_perm;        // [R*d] elements (at least (R+S*T)*d bytes: the W8A8 grouped row codes)
   size_t h;             // [(R+S*T)*F] elements: silu(gate) * up
   size_t y;             // [(R+S*T)*d] elements: expert outputs; with the fused combine, the
                         // [T*d] float32 output accumulator instead (the region holds either);
                         // in the W8A8 layer first the E4M3 codes of the expert inputs [(R+S*T)*d]
   size_t a8_scale;      // [R+S*T] float: W8A8 per-row scales of the expert inputs
-  size_t xq_scale;      // [T] float: W8A8 per-token scales (the per-token codes use the x_perm region)
+  size_t xq_scale;      // [T] float: W8A8 per-token scales (the per-token codes use the y region)
   size_t h8;            // [(R+S*T)*F] bytes: W8A8 E4M3 codes of h
   size_t h8_scale;      // [R+S*T] float: their per-row scales
-  size_t mlp_ready;     // [m-tiles] int32: the one-launch expert MLP's per-m-tile h counters
+  size_t mlp_ready;     // [2 * m-tiles] int32: the one-launch expert MLP's per-m-tile counters
   size_t total;
 };
 
@@ -88,8 +88,11 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 cudaError_t launch_router_fma(const Shape& s, const void* x, const void* w, const float* bias,
                               int32_t* idx, float* gate, float* scores, cudaStream_t st);
 bool router_tc_supported(const Shape& s);
+// pf0 / pf1 / pf_bytes (batches of at most 128 tokens): two byte ranges the router prefetches
+// into L2 while it runs, 16-byte aligned, pf_bytes a multiple of 16; 0 for none.
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const float* bias,
-                             int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st);
+                             int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st,
+                             const void* pf0 = nullptr, const void* pf1 = nullptr, uint64_t pf_bytes = 0);
 
 cudaError_t launch_group_hist(const Shape& s, const int32_t* idx, int32_t* chunk_counts,
                               int32_t* status, cudaStream_t st);
@@ -152,6 +155,13 @@ int64_t fused_mlp_ready_ints(const Shape& s);
 cudaError_t launch_mlp_fused_tc(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
                                 const void* w_up, const void* w_down, const void* sched, void* h, void* y,
                                 int32_t* ready, int32_t* status, cudaStream_t st);
+
+// The W8A8 expert MLP in one persistent launch (gemm_w8a8_fused.cu); `counters` holds
+// 2 * fused_mlp_ready_ints(s) int32 (zeroed by the launcher).
+cudaError_t launch_mlp_w8a8_fused(const Shape& s, const uint8_t* x8, const float* x8_scale, const uint8_t* wg_q,
+                                  const float* wg_s, const uint8_t* wu_q, const float* wu_s, const uint8_t* wd_q,
+                                  const float* wd_s, const void* sched, void* h, uint8_t* h8, float* h8_scale,
+                                  void* y, int32_t* counters, int32_t* status, cudaStream_t st);
 
 // W8A8 (E4M3 weights and activations, gemm_w8a8.cu).
 bool w8a8_supported(const Shape& s);

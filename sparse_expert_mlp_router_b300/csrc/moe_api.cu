@@ -117,20 +117,24 @@ WsLayout make_layout(const Shape& s) {
   L.sched = take((size_t)4 * (s.G + 1) * 4);
   L.dest_row = take(pairs * 4);
   L.src_token = take((size_t)s.R * 4);
-  // x_perm also holds the W8A8 layer's per-token codes [T, d] (bytes)
+  // x_perm holds the W8A8 layer's grouped E4M3 rows [R + S*T, d] (bytes) instead of the bf16
+  // rows: nothing in the expert stage writes it, so the one-launch MLP's gate/up tiles can read
+  // the codes while its down tiles already write y
   size_t xp_bytes = (size_t)s.R * s.d * s.esize;
-  if (s.dtype == MOE_BF16 && xp_bytes < (size_t)s.T * s.d) xp_bytes = (size_t)s.T * s.d;
+  if (s.dtype == MOE_BF16 && xp_bytes < grouped * s.d) xp_bytes = grouped * s.d;
   L.x_perm = take(xp_bytes);
   L.h = take(grouped * s.F * s.esize);
+  // y also holds the fused combine's float32 sums [T, d] and, during the grouping stage of a
+  // multi-chunk W8A8 layer, the per-token E4M3 codes [T, d] (bytes)
   size_t y_bytes = grouped * s.d * s.esize;
-  if (s.dtype == MOE_BF16 && y_bytes < (size_t)s.T * s.d * 4) y_bytes = (size_t)s.T * s.d * 4;   // fused combine
+  if (s.dtype == MOE_BF16 && y_bytes < (size_t)s.T * s.d * 4) y_bytes = (size_t)s.T * s.d * 4;
   L.y = take(y_bytes);
   if (s.dtype == MOE_BF16) {
     L.a8_scale = take(grouped * 4);
     L.xq_scale = take((size_t)s.T * 4);
     L.h8 = take(grouped * s.F);
     L.h8_scale = take(grouped * 4);
-    L.mlp_ready = take((size_t)fused_mlp_ready_ints(s) * 4);
+    L.mlp_ready = take((size_t)2 * fused_mlp_ready_ints(s) * 4);
   }
   L.total = o;
   return L;
@@ -166,9 +170,12 @@ moe_status_t check_ws(const Shape& s, const void* ws, size_t ws_bytes) {
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // The stage bodies, shared by the stage entry points and the whole-layer call.
+// pf0 / pf1 / pf_bytes: the L2 warm-up ranges of the whole-layer call (see l2_warm_bytes).
 cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
-                       float* gate, float* scores, int32_t* status, cudaStream_t st) {
-  if (router_tc_supported(s)) return launch_router_tc(s, x, w_router, bias, idx, gate, scores, status, st);
+                       float* gate, float* scores, int32_t* status, cudaStream_t st, const void* pf0 = nullptr,
+                       const void* pf1 = nullptr, uint64_t pf_bytes = 0) {
+  if (router_tc_supported(s))
+    return launch_router_tc(s, x, w_router, bias, idx, gate, scores, status, st, pf0, pf1, pf_bytes);
   return launch_router_fma(s, x, w_router, bias, idx, gate, scores, st);
 }
 
@@ -193,8 +200,8 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
       return e;
     if ((e = launch_group_scatter(s, idx, cc, offsets, dest_row, src_token, st)) != cudaSuccess) return e;
   }
-  if (x8 != nullptr)   // per-token codes (multi-chunk batches) go to the unused x_perm region
-    return launch_gather_quant_rows(s, x, src_token, offsets, x8, x8s, static_cast<uint8_t*>(x_perm),
+  if (x8 != nullptr)   // per-token codes (multi-chunk batches) go to the y region, free until the down projection
+    return launch_gather_quant_rows(s, x, src_token, offsets, x8, x8s, at<uint8_t>(ws, L.y),
                                     at<float>(ws, L.xq_scale), st);
   return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
 }
@@ -215,6 +222,15 @@ bool fused_mlp(const Shape& s) {
   const char* v = getenv("MOE_FUSED_MLP");
   if (v != nullptr && (v[0] == '0' || v[0] == '1')) return v[0] == '1';
   return s.nchunks == 1;
+}
+
+// The W8A8 expert MLP as one launch (gate/up, h's quantisation by the tile that completes each
+// m-tile, down) only when MOE_FUSED_MLP=1: it measured slower than the three launches on every
+// shape (decode 0.137 vs 0.132 ms, Qwen3-shaped 1.61 vs 0.48, DeepSeek-shaped 2.95 vs 2.27).
+bool fused_mlp_w8a8(const Shape& s) {
+  if (!fused_mlp_supported(s)) return false;
+  const char* v = getenv("MOE_FUSED_MLP");
+  return v != nullptr && v[0] == '1';
 }
 
 // Expert weights of a call: bf16 / float32 tensors, or FP8 codes with per-row scales.
@@ -278,13 +294,41 @@ bool fused_combine(const Shape& s, const ExpertWeights& w) {
   return v != nullptr && v[0] == '1';
 }
 
-// Kernel launches one moe_layer_forward enqueues.
-int layer_launches(const Shape& s) {
-  // hist, scan (+ group schedule), scatter, gather; one CTA for the first three when the batch
-  // is a single chunk of tokens
-  const int router = 1, grouping = s.nchunks == 1 ? 2 : 4, mlp = (s.dtype == MOE_BF16 && fused_mlp(s)) ? 1 : 2,
-            combine = 1;
-  return router + grouping + mlp + combine;
+// L2 warm-up of a one-chunk batch (decode). The router and grouping of up to 128 tokens move
+// under a megabyte and leave HBM idle for tens of microseconds, after which the expert MLP
+// streams the touched experts' weights, its first round of tiles the gate/up rows of the
+// lowest-index experts. So the router kernel prefetches into L2 the W_gate and W_up of experts
+// 0 .. n-1, n = budget / (bytes of one expert's W_gate + W_up): pf_bytes of each tensor (0 for
+// none). An expert the batch does not touch is read for nothing, in time HBM had free. Budget:
+// MOE_L2_WARM_MB in the environment (read at every call; 0 turns it off), else the default.
+// weights: 0 bf16, else E4M3 codes (one byte per weight).
+constexpr int64_t kL2WarmMbDefault = 64;
+uint64_t l2_warm_bytes(const Shape& s, int weights) {
+  if (s.nchunks != 1 || s.dtype != MOE_BF16 || !router_tc_supported(s)) return 0;
+  int64_t mb = kL2WarmMbDefault;
+  const char* v = getenv("MOE_L2_WARM_MB");
+  if (v != nullptr && *v != 0) mb = strtoll(v, nullptr, 10);
+  if (mb <= 0) return 0;
+  if (mb > 1024) mb = 1024;
+  const uint64_t per = (uint64_t)s.F * s.d * (weights != 0 ? 1 : 2);
+  uint64_t n = ((uint64_t)mb << 20) / (2 * per);
+  if (n > (uint64_t)s.E) n = (uint64_t)s.E;
+  return n * per;
+}
+
+// Kernel launches one layer call enqueues; weights: 0 bf16 / float32, 1 FP8 codes with bf16
+// activations, 2 W8A8. Memset nodes are not counted.
+int layer_launches(const Shape& s, int weights) {
+  // grouping: hist, scan (+ group schedule), scatter, row copy (W8A8: per-token quantiser and
+  // code-row copy); one CTA for the first three when the batch is a single chunk of tokens
+  int grouping = s.nchunks == 1 ? 2 : 4;
+  if (weights == 2 && s.nchunks != 1) grouping += 1;
+  int mlp = 2;
+  ExpertWeights w{nullptr, nullptr, nullptr};
+  w.fp8 = weights != 0;
+  if (weights == 2) mlp = fused_mlp_w8a8(s) ? 1 : 3;                 // + the quantiser of h
+  else if (weights == 0 && s.dtype == MOE_BF16 && !fused_combine(s, w) && fused_mlp(s)) mlp = 1;
+  return 1 /*router*/ + grouping + mlp + 1 /*combine*/;
 }
 
 moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
@@ -323,14 +367,15 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   if (!mark(0)) return MOE_ERR_CUDA;
   {
     const NvtxRange r("moe_layer/router");
-    if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
+    const uint64_t pf = l2_warm_bytes(s, w.fp8 ? 1 : 0);
+    if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st, w.g, w.u, pf) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   if (!mark(1)) return MOE_ERR_CUDA;
   {
     const NvtxRange r("moe_layer/grouping");
-    // W8A8: the grouped x rows go straight to E4M3 codes in the y region (free until the down
-    // projection writes y)
-    uint8_t* x8 = w.a8 ? at<uint8_t>(ws, L.y) : nullptr;
+    // W8A8: the grouped x rows go straight to E4M3 codes in the x_perm region
+    uint8_t* x8 = w.a8 ? at<uint8_t>(ws, L.x_perm) : nullptr;
     float* x8s = w.a8 ? at<float>(ws, L.a8_scale) : nullptr;
     if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st, x8, x8s) !=
         cudaSuccess)
@@ -345,22 +390,31 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
       // gate/up on the codes of the grouping stage, h -> codes, down on codes
       void* sched = at<void>(ws, L.sched);
       void* h = at<void>(ws, L.h);
-      uint8_t* x8 = at<uint8_t>(ws, L.y);
+      uint8_t* x8 = at<uint8_t>(ws, L.x_perm);
       float* x8s = at<float>(ws, L.a8_scale);
       uint8_t* h8 = at<uint8_t>(ws, L.h8);
       float* h8s = at<float>(ws, L.h8_scale);
       const int64_t n_sh = (int64_t)s.S * s.T;
-      if (launch_gemm_gateup_w8a8(s, x8, x8s, static_cast<const uint8_t*>(w.g), w.gs, static_cast<const uint8_t*>(w.u),
-                                  w.us, sched, h, status, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      if (!mark(3)) return MOE_ERR_CUDA;
-      const void* h_shared = n_sh ? static_cast<const void*>(static_cast<const char*>(h) + (size_t)s.R * s.F * 2)
-                                  : nullptr;
-      if (launch_quantize_act_rows(s, h, offsets + s.E, s.R, h_shared, n_sh, s.F, h8, h8s, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      if (launch_gemm_down_w8a8(s, h8, h8s, static_cast<const uint8_t*>(w.d), w.ds, sched, y, status, st) !=
-          cudaSuccess)
-        return MOE_ERR_CUDA;
+      if (fused_mlp_w8a8(s)) {
+        // both contractions and h's quantisation in one launch; the stage boundary event falls before it
+        if (!mark(3)) return MOE_ERR_CUDA;
+        if (launch_mlp_w8a8_fused(s, x8, x8s, static_cast<const uint8_t*>(w.g), w.gs, static_cast<const uint8_t*>(w.u),
+                                  w.us, static_cast<const uint8_t*>(w.d), w.ds, sched, h, h8, h8s, y,
+                                  at<int32_t>(ws, L.mlp_ready), status, st) != cudaSuccess)
+          return MOE_ERR_CUDA;
+      } else {
+        if (launch_gemm_gateup_w8a8(s, x8, x8s, static_cast<const uint8_t*>(w.g), w.gs,
+                                    static_cast<const uint8_t*>(w.u), w.us, sched, h, status, st) != cudaSuccess)
+          return MOE_ERR_CUDA;
+        if (!mark(3)) return MOE_ERR_CUDA;
+        const void* h_shared = n_sh ? static_cast<const void*>(static_cast<const char*>(h) + (size_t)s.R * s.F * 2)
+                                    : nullptr;
+        if (launch_quantize_act_rows(s, h, offsets + s.E, s.R, h_shared, n_sh, s.F, h8, h8s, st) != cudaSuccess)
+          return MOE_ERR_CUDA;
+        if (launch_gemm_down_w8a8(s, h8, h8s, static_cast<const uint8_t*>(w.d), w.ds, sched, y, status, st) !=
+            cudaSuccess)
+          return MOE_ERR_CUDA;
+      }
     } else if (fused) {
       void* sched = at<void>(ws, L.sched);
       void* h = at<void>(ws, L.h);
@@ -581,13 +635,35 @@ moe_status_t moe_layer_forward_timed(const moe_config_t* cfg, const void* x, con
 
 int32_t moe_layer_launch_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return -1;
-  return layer_launches(make_shape(*cfg));
+  return layer_launches(make_shape(*cfg), 0);
+}
+
+int32_t moe_layer_launch_count_weights(const moe_config_t* cfg, int32_t weights) {
+  if (check_cfg(cfg) != MOE_OK || weights < 0 || weights > 2) return -1;
+  const Shape s = make_shape(*cfg);
+  if (weights != 0 && !fp8w_supported(s)) return -1;
+  return layer_launches(s, weights);
+}
+
+int64_t moe_layer_l2_warm_bytes(const moe_config_t* cfg, int32_t weights) {
+  if (check_cfg(cfg) != MOE_OK || weights < 0 || weights > 2) return -1;
+  const Shape s = make_shape(*cfg);
+  if (weights != 0 && !fp8w_supported(s)) return -1;
+  return (int64_t)(2 * l2_warm_bytes(s, weights));
 }
 
 int32_t moe_layer_mlp_fused(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return -1;
   const Shape s = make_shape(*cfg);
   return (s.dtype == MOE_BF16 && fused_mlp(s)) ? 1 : 0;
+}
+
+int32_t moe_layer_mlp_fused_weights(const moe_config_t* cfg, int32_t weights) {
+  if (check_cfg(cfg) != MOE_OK || weights < 0 || weights > 2) return -1;
+  const Shape s = make_shape(*cfg);
+  if (weights != 0 && !fp8w_supported(s)) return -1;
+  if (weights == 1 || s.dtype != MOE_BF16) return 0;
+  return (weights == 2 ? fused_mlp_w8a8(s) : fused_mlp(s)) ? 1 : 0;
 }
 
 moe_status_t moe_selftest_bounded_wait(void* ws, size_t ws_bytes, uint64_t limit_ns, cudaStream_t stream) {

@@ -156,3 +156,17 @@ def test_fused_mlp_layer_writes_only_its_outputs(name, edit, monkeypatch):
                           bufs["out"].t, bufs["workspace"].t)
     assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
     _check_all(bufs, f"fused mlp layer {name}")
+
+
+@pytest.mark.parametrize("name,edit", [("mini_decode", {}), ("mini_deepseek", {})])
+def test_w8a8_one_launch_layer_writes_only_its_outputs(name, edit, monkeypatch):
+    monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    w = synth.WORKLOADS[name].with_(**edit)
+    dev = Inputs(w).device()
+    cfg = cfg_of(w)
+    q = {n: moe.moe_quantize_fp8_rows(dev[n]) for n in ("w_gate", "w_up", "w_down")}
+    bufs = {"out": Guarded((w.T, w.d_model), torch.bfloat16), "workspace": _workspace(cfg)}
+    moe.moe_layer_forward_w8a8(cfg, dev["x"], dev["w_router"], dev["bias"], *q["w_gate"], *q["w_up"], *q["w_down"],
+                               bufs["out"].t, bufs["workspace"].t)
+    assert moe.moe_get_device_error(bufs["workspace"].t) == moe.MOE_OK
+    _check_all(bufs, f"w8a8 one-launch layer {name}")

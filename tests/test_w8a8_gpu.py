@@ -127,3 +127,22 @@ def test_w8a8_refuses_shapes_it_does_not_take(edit, dtype):
         moe.moe_layer_forward_w8a8(cfg, dev["x"], dev["w_router"], dev["bias"], *q["w_gate"], *q["w_up"],
                                    *q["w_down"], out, ws)
     assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name,edit", [("mini_decode", {}), ("mini_deepseek", {}), ("mini_qwen3", {}),
+                                       ("mini_mixtral", {"T": 1200}), ("mini_deepseek", {"capacity_factor": 0.05}),
+                                       ("decode_qwen3", {})])
+def test_w8a8_one_launch_mlp_is_bit_identical(name, edit, monkeypatch):
+    # MOE_FUSED_MLP=1: gate/up tiles, h's per-row quantisation by the tile that completes each
+    # 128-row block, and the down tiles in one launch (the default for single-chunk batches);
+    # =0: three launches. Same arithmetic: the outputs agree bit for bit.
+    w = synth.WORKLOADS[name].with_(**edit)
+    dev = synth.device_inputs(w) if not name.startswith("mini") else Inputs(w).device()
+    cfg = cfg_of(w)
+    qw = {n: moe.moe_quantize_fp8_rows(dev[n]) for n in ("w_gate", "w_up", "w_down")}
+    outs = []
+    for mode in ("0", "1", "1"):                                 # twice with one launch: counters restart
+        monkeypatch.setenv("MOE_FUSED_MLP", mode)
+        outs.append(_run(w, dev, {n: (*qw[n], None) for n in qw}, cfg))
+    assert all((o[1] == outs[0][1]).all() for o in outs[1:])
+    assert all(torch.equal(o[0].view(torch.int16), outs[0][0].view(torch.int16)) for o in outs[1:])
