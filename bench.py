@@ -751,18 +751,6 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
                                         "w8a8" if a8 else "fp8" if fp8 else "bf16")
                        if w.dtype == "bf16" else None)
     roof["ms_per_launch"] = gemm_ms
-    # decode-shaped batches: the router prefetched the first experts' W_gate / W_up into L2, so
-    # that many of the kernel's algorithmic bytes came from L2 (read from HBM during routing);
-    # the kernel's rate without them is reported beside it, the whole layer's in layer_roofline_frac
-    warm = moe.moe_layer_l2_warm_bytes(cfg, weights if fp8 else "bf16") if w.dtype == "bf16" else 0
-    roof["l2_warm_bytes"] = warm
-    if warm > 0 and roof["bound"] == "hbm":
-        # W_gate + W_up of experts 0 .. n-1; those of the experts the batch touched are in r_bytes
-        per_expert = 2.0 * w.d_ff * w.d_model * (1.0 if fp8 else 2.0)
-        n_warm = int(round(warm / per_expert))
-        used = float((np.minimum(c, cap)[:n_warm] > 0).sum()) * per_expert
-        roof["l2_warm_bytes_touched"] = used
-        roof["frac_without_warm_bytes"] = (r_bytes - used) / (gemm_ms / 1e3) / 1e9 / roof["peak"]
 
     stages_ms = dict(zip(["router", "grouping", "gemm_gate_up", "gemm_down", "combine"],
                          [float(v) for v in stage.mean(axis=0)]))

@@ -361,19 +361,6 @@ int32_t moe_layer_mlp_fused(const moe_config_t* cfg);
 int32_t moe_layer_mlp_fused_weights(const moe_config_t* cfg, int32_t weights);
 
 /*
- * Bytes of expert weights the whole-layer call on `cfg` prefetches into L2 while its router
- * runs (0 if none), with `weights` as in moe_layer_launch_count_weights; -1 for an invalid
- * config or a weights mode the shape does not take. A batch of at most 128 tokens (decode)
- * leaves HBM idle during routing and grouping, after which the expert MLP streams the touched
- * experts' weights, its first tiles the gate/up rows of the lowest-index experts; so the
- * router prefetches W_gate and W_up of experts 0 .. n-1, as many as fit the budget
- * (MOE_L2_WARM_MB in the environment, read at every call, 0 = off; default 64 MB). A hint
- * only: results do not depend on it. Mixture-of-Experts pages, "Memory vs compute,
- * quantified" (decode reads each touched expert's weights once).
- */
-int64_t moe_layer_l2_warm_bytes(const moe_config_t* cfg, int32_t weights);
-
-/*
  * Synchronise `stream`, then return the first device-side status recorded in the workspace
  * since the last moe_workspace_init / moe_clear_device_error (MOE_OK if none).
  */

@@ -23,7 +23,7 @@ EXPORTS = [
     "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_get_device_error",
     "moe_clear_device_error", "moe_selftest_bounded_wait", "moe_layer_launch_count", "moe_layer_mlp_fused",
-    "moe_layer_launch_count_weights", "moe_layer_l2_warm_bytes", "moe_layer_mlp_fused_weights",
+    "moe_layer_launch_count_weights", "moe_layer_mlp_fused_weights",
     "moe_permute_noalloc", "moe_routing_stats", "moe_quantize_fp8_rows", "moe_grouped_ffn_fp8",
     "moe_layer_forward_fp8", "moe_layer_forward_fp8_timed", "moe_layer_forward_w8a8", "moe_layer_forward_w8a8_timed",
 ]
@@ -98,7 +98,6 @@ def lib() -> ctypes.CDLL:
             "moe_layer_launch_count": ([_cfgp], i32),
             "moe_layer_mlp_fused": ([_cfgp], i32),
             "moe_layer_launch_count_weights": ([_cfgp, i32], i32),
-            "moe_layer_l2_warm_bytes": ([_cfgp, i32], i64),
             "moe_layer_mlp_fused_weights": ([_cfgp, i32], i32),
             "moe_permute_noalloc": ([_cfgp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], i32),
             "moe_routing_stats": ([_cfgp, _vp, _vp, _vp], i32),
@@ -180,11 +179,6 @@ def moe_layer_launch_count_weights(cfg: MoeConfig, weights: str) -> int:
 
 def moe_layer_mlp_fused_weights(cfg: MoeConfig, weights: str) -> int:
     return lib().moe_layer_mlp_fused_weights(ctypes.byref(cfg), WEIGHTS_MODE[weights])
-
-
-def moe_layer_l2_warm_bytes(cfg: MoeConfig, weights: str = "bf16") -> int:
-    """Expert-weight bytes the whole-layer call prefetches into L2 during routing (0: none)."""
-    return lib().moe_layer_l2_warm_bytes(ctypes.byref(cfg), WEIGHTS_MODE[weights])
 
 
 # -------------------------------------------------------------- workspace

@@ -88,11 +88,8 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 cudaError_t launch_router_fma(const Shape& s, const void* x, const void* w, const float* bias,
                               int32_t* idx, float* gate, float* scores, cudaStream_t st);
 bool router_tc_supported(const Shape& s);
-// pf0 / pf1 / pf_bytes (batches of at most 128 tokens): two byte ranges the router prefetches
-// into L2 while it runs, 16-byte aligned, pf_bytes a multiple of 16; 0 for none.
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const float* bias,
-                             int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st,
-                             const void* pf0 = nullptr, const void* pf1 = nullptr, uint64_t pf_bytes = 0);
+                             int32_t* idx, float* gate, float* scores, int32_t* status, cudaStream_t st);
 
 cudaError_t launch_group_hist(const Shape& s, const int32_t* idx, int32_t* chunk_counts,
                               int32_t* status, cudaStream_t st);

@@ -170,12 +170,9 @@ moe_status_t check_ws(const Shape& s, const void* ws, size_t ws_bytes) {
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // The stage bodies, shared by the stage entry points and the whole-layer call.
-// pf0 / pf1 / pf_bytes: the L2 warm-up ranges of the whole-layer call (see l2_warm_bytes).
 cudaError_t run_router(const Shape& s, const void* x, const void* w_router, const float* bias, int32_t* idx,
-                       float* gate, float* scores, int32_t* status, cudaStream_t st, const void* pf0 = nullptr,
-                       const void* pf1 = nullptr, uint64_t pf_bytes = 0) {
-  if (router_tc_supported(s))
-    return launch_router_tc(s, x, w_router, bias, idx, gate, scores, status, st, pf0, pf1, pf_bytes);
+                       float* gate, float* scores, int32_t* status, cudaStream_t st) {
+  if (router_tc_supported(s)) return launch_router_tc(s, x, w_router, bias, idx, gate, scores, status, st);
   return launch_router_fma(s, x, w_router, bias, idx, gate, scores, st);
 }
 
@@ -294,28 +291,6 @@ bool fused_combine(const Shape& s, const ExpertWeights& w) {
   return v != nullptr && v[0] == '1';
 }
 
-// L2 warm-up of a one-chunk batch (decode). The router and grouping of up to 128 tokens move
-// under a megabyte and leave HBM idle for tens of microseconds, after which the expert MLP
-// streams the touched experts' weights, its first round of tiles the gate/up rows of the
-// lowest-index experts. So the router kernel prefetches into L2 the W_gate and W_up of experts
-// 0 .. n-1, n = budget / (bytes of one expert's W_gate + W_up): pf_bytes of each tensor (0 for
-// none). An expert the batch does not touch is read for nothing, in time HBM had free. Budget:
-// MOE_L2_WARM_MB in the environment (read at every call; 0 turns it off), else the default.
-// weights: 0 bf16, else E4M3 codes (one byte per weight).
-constexpr int64_t kL2WarmMbDefault = 64;
-uint64_t l2_warm_bytes(const Shape& s, int weights) {
-  if (s.nchunks != 1 || s.dtype != MOE_BF16 || !router_tc_supported(s)) return 0;
-  int64_t mb = kL2WarmMbDefault;
-  const char* v = getenv("MOE_L2_WARM_MB");
-  if (v != nullptr && *v != 0) mb = strtoll(v, nullptr, 10);
-  if (mb <= 0) return 0;
-  if (mb > 1024) mb = 1024;
-  const uint64_t per = (uint64_t)s.F * s.d * (weights != 0 ? 1 : 2);
-  uint64_t n = ((uint64_t)mb << 20) / (2 * per);
-  if (n > (uint64_t)s.E) n = (uint64_t)s.E;
-  return n * per;
-}
-
 // Kernel launches one layer call enqueues; weights: 0 bf16 / float32, 1 FP8 codes with bf16
 // activations, 2 W8A8. Memset nodes are not counted.
 int layer_launches(const Shape& s, int weights) {
@@ -367,9 +342,7 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   if (!mark(0)) return MOE_ERR_CUDA;
   {
     const NvtxRange r("moe_layer/router");
-    const uint64_t pf = l2_warm_bytes(s, w.fp8 ? 1 : 0);
-    if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st, w.g, w.u, pf) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (run_router(s, x, w_router, bias, idx, gate, nullptr, status, st) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (!mark(1)) return MOE_ERR_CUDA;
   {
@@ -643,13 +616,6 @@ int32_t moe_layer_launch_count_weights(const moe_config_t* cfg, int32_t weights)
   const Shape s = make_shape(*cfg);
   if (weights != 0 && !fp8w_supported(s)) return -1;
   return layer_launches(s, weights);
-}
-
-int64_t moe_layer_l2_warm_bytes(const moe_config_t* cfg, int32_t weights) {
-  if (check_cfg(cfg) != MOE_OK || weights < 0 || weights > 2) return -1;
-  const Shape s = make_shape(*cfg);
-  if (weights != 0 && !fp8w_supported(s)) return -1;
-  return (int64_t)(2 * l2_warm_bytes(s, weights));
 }
 
 int32_t moe_layer_mlp_fused(const moe_config_t* cfg) {

@@ -78,13 +78,7 @@ struct RouterArgs {
   float* gate;
   float* scores;
   int32_t* status;
-  // L2 warm-up (one-tile batches): two byte ranges of pf_bytes each, prefetched into L2 while
-  // the router runs (the expert weights the MLP reads first)
-  const uint8_t* pf0;
-  const uint8_t* pf1;
-  uint64_t pf_bytes;
 };
-constexpr uint32_t kPrefetchChunk = 16384;
 
 __device__ __forceinline__ bool ranks_before(float a, int ea, float b, int eb) {
   return a > b || (a == b && ea < eb);
@@ -283,17 +277,6 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const int quarter = warp & 3;                     // the TMEM lanes this warp may read
     const int slice0 = (warp - 2) >> 2;               // first 32-column slice of this warp
     const int r = quarter * 32 + lane;                // row of the tile = TMEM lane
-    if (warp == 2 && a.pf_bytes > 0) {
-      // this CTA's share of the warm-up: chunks i = crank, crank + C, ... of the two ranges
-      // interleaved (chunk j of range 0, chunk j of range 1, ...); the loads complete on their own
-      const uint64_t nch = (a.pf_bytes + kPrefetchChunk - 1) / kPrefetchChunk;
-      for (uint64_t i = (uint64_t)crank + (uint64_t)C * lane; i < 2 * nch; i += (uint64_t)C * 32) {
-        const uint64_t off = (i >> 1) * kPrefetchChunk;
-        const uint64_t left = a.pf_bytes - off;
-        ptx::bulk_prefetch_l2(((i & 1) ? a.pf1 : a.pf0) + off,
-                              (uint32_t)(left < kPrefetchChunk ? left : kPrefetchChunk));
-      }
-    }
     if (!ptx::mbar_wait_bounded(ptx::smem_u32(tfull), 0, abort_flag, kWaitLimitNs)) {
       set_status(a.status, MOE_ERR_TIMEOUT);
       *abort_flag = 1;
@@ -548,13 +531,8 @@ bool router_tc_supported(const Shape& s) {
 }
 
 cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const float* bias, int32_t* idx,
-                             float* gate, float* scores, int32_t* status, cudaStream_t st, const void* pf0,
-                             const void* pf1, uint64_t pf_bytes) {
+                             float* gate, float* scores, int32_t* status, cudaStream_t st) {
   if (!router_tc_supported(s)) return cudaErrorInvalidValue;
-  // the warm-up ranges: one-tile batches only, 16-byte aligned addresses and size
-  if (pf_bytes > 0 && (s.T > kBM || pf0 == nullptr || pf1 == nullptr || pf_bytes % 16 != 0 ||
-                       reinterpret_cast<uintptr_t>(pf0) % 16 != 0 || reinterpret_cast<uintptr_t>(pf1) % 16 != 0))
-    return cudaErrorInvalidValue;
   RouterArgs a{};
   a.T = s.T;
   a.E = s.E;
@@ -585,9 +563,6 @@ cudaError_t launch_router_tc(const Shape& s, const void* x, const void* w, const
   a.gate = gate;
   a.scores = scores;
   a.status = status;
-  a.pf0 = static_cast<const uint8_t*>(pf0);
-  a.pf1 = static_cast<const uint8_t*>(pf1);
-  a.pf_bytes = pf_bytes;
   CUtensorMap tx, tw;
   if (!make_tmap_bf16(&tx, x, (uint64_t)s.d, (uint64_t)s.T, kBM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tw, w, (uint64_t)s.d, (uint64_t)s.E, (uint32_t)a.N)) return cudaErrorInvalidValue;

@@ -112,13 +112,6 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// Bulk prefetch of `bytes` of global memory into L2 (no destination, no completion): address
-// and size multiples of 16 bytes.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
-}
-
 // 2D tiled load of box {c0 .. c0+box0, c1 .. c1+box1} into shared memory, completing
 // `bytes` of transaction count on mbarrier `bar`. c0 is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, uint32_t bar) {

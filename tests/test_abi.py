@@ -180,19 +180,3 @@ def test_launch_count_follows_the_grouping_path(monkeypatch):
     assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 2 + 1 + 1
     assert moe.moe_layer_launch_count_weights(_cfg(T=129), "w8a8") == 1 + 5 + 1 + 1
 
-
-def test_l2_warm_up_covers_whole_experts_within_the_budget(monkeypatch):
-    # one-chunk batches only: W_gate and W_up of the first n experts, n = budget // (2 * F * d * bytes)
-    monkeypatch.delenv("MOE_L2_WARM_MB", raising=False)
-    c = _cfg(T=32, d_model=2048, n_experts=128, top_k=8, d_ff=768)
-    per = 768 * 2048
-    assert moe.moe_layer_l2_warm_bytes(c, "bf16") == 2 * ((64 << 20) // (4 * per)) * 2 * per
-    assert moe.moe_layer_l2_warm_bytes(c, "fp8") == 2 * ((64 << 20) // (2 * per)) * per
-    assert moe.moe_layer_l2_warm_bytes(c, "w8a8") == moe.moe_layer_l2_warm_bytes(c, "fp8")
-    assert moe.moe_layer_l2_warm_bytes(_cfg(T=129, d_model=2048, n_experts=128, top_k=8, d_ff=768)) == 0
-    assert moe.moe_layer_l2_warm_bytes(_cfg(T=32, dtype="f32")) == 0
-    assert moe.moe_layer_l2_warm_bytes(_cfg(top_k=300)) == -1
-    monkeypatch.setenv("MOE_L2_WARM_MB", "0")
-    assert moe.moe_layer_l2_warm_bytes(c, "bf16") == 0
-    monkeypatch.setenv("MOE_L2_WARM_MB", "100000")      # clamped to 1 GB, then to all experts
-    assert moe.moe_layer_l2_warm_bytes(c, "bf16") == 128 * 2 * per * 2
