@@ -826,6 +826,9 @@ def run_ours(args, w):
         "grouped_gemm_frac_of_burst": head["grouped_gemm_frac_of_burst"],
         "expert_weight_frac_of_hbm": head["expert_weight_frac_of_hbm"],
     }
+    for key in ("expert_weight_gbs", "grouped_gemm_frac_of_sustained", "expert_weight_frac_of_nominal_hbm",
+                "layer_roofline_frac"):
+        line[key] = head[key]
     if "w8a8" in head:
         line["w8a8"] = head["w8a8"]
     if extras:
