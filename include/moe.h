@@ -233,7 +233,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int3
 
 /*
  * The whole layer: router -> permute -> grouped MLPs -> combine, enqueued on `stream`
- * with no host synchronisation (capturable in a CUDA graph).
+ * with no host synchronisation (capturable in a CUDA graph). A float32 layer's expert MLP
+ * reads the routed rows from x through src_token, so its permute writes no x_perm copy (the
+ * same values as the stage calls).
  *   out            device [T, d_model] out: the MoE FFN output (no residual add)
  *   topk_idx_out   device [T, k] int32 out or NULL (routing is then kept in the workspace)
  *   counts_out     device [E] int32 out or NULL (per-expert load before capacity)

@@ -63,10 +63,12 @@ __device__ __forceinline__ float quad_sum(float v) {
   return v;
 }
 
+// A routed group's rows are read from x_perm, or (src_token non-NULL: the whole-layer call,
+// which then skips the grouped copy) from x through src_token: the same values.
 __global__ void ffn_gateup_fma_kernel(const float* __restrict__ x_perm, const float* __restrict__ x,
-                                      const float* __restrict__ wg, const float* __restrict__ wu,
-                                      const int32_t* __restrict__ sched, int G, int E, int d, int F,
-                                      int64_t n_rows, float* __restrict__ h) {
+                                      const int32_t* __restrict__ src_token, const float* __restrict__ wg,
+                                      const float* __restrict__ wu, const int32_t* __restrict__ sched, int G, int E,
+                                      int d, int F, int64_t n_rows, float* __restrict__ h) {
   const int p = threadIdx.x & (kQuad - 1);
   const int64_t total = n_rows * F;
   const int64_t stride = (int64_t)gridDim.x * (blockDim.x / kQuad);
@@ -85,8 +87,11 @@ __global__ void ffn_gateup_fma_kernel(const float* __restrict__ x_perm, const fl
       g = row_group(sched, G, r, local);
       if (g >= 0) {
         const int32_t* a_row = sched + (G + 1);
-        const float4* a = reinterpret_cast<const float4*>((g >= E) ? x + (size_t)(a_row[g] + local) * d
-                                                                   : x_perm + (size_t)(a_row[g] + local) * d);
+        const int arow = a_row[g] + local;
+        const float* base = (g >= E) ? x + (size_t)arow * d
+                            : src_token ? x + (size_t)src_token[arow] * d
+                                        : x_perm + (size_t)arow * d;
+        const float4* a = reinterpret_cast<const float4*>(base);
         const float4* wgr = reinterpret_cast<const float4*>(wg + ((size_t)g * F + f) * d);
         const float4* wur = reinterpret_cast<const float4*>(wu + ((size_t)g * F + f) * d);
         for (int v = p; v < nv; v += kQuad) {
@@ -146,7 +151,7 @@ cudaError_t launch_group_schedule(const Shape& s, const int32_t* offsets, void* 
 // The two float32 MLP kernels; mid_event (nullable) is recorded between them.
 cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, const void* w_gate, const void* w_up,
                            const void* w_down, const void* sched, void* h, void* y, cudaStream_t st,
-                           cudaEvent_t mid_event) {
+                           cudaEvent_t mid_event, const int32_t* src_token) {
   const int64_t n_rows = s.R + (int64_t)s.S * s.T;
   const int threads = 256;                      // 64 output elements per block (four lanes each)
   const int64_t per_block = threads / 4;
@@ -158,7 +163,7 @@ cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, co
   const int32_t* sc = static_cast<const int32_t*>(sched);
   // float32 layers only; bf16 layers run on the tensor cores
   ffn_gateup_fma_kernel<<<(unsigned)b1, threads, 0, st>>>(
-      static_cast<const float*>(x_perm), static_cast<const float*>(x), static_cast<const float*>(w_gate),
+      static_cast<const float*>(x_perm), static_cast<const float*>(x), src_token, static_cast<const float*>(w_gate),
       static_cast<const float*>(w_up), sc, s.G, s.E, s.d, s.F, n_rows, static_cast<float*>(h));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

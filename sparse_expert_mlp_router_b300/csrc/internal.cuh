@@ -108,10 +108,11 @@ cudaError_t launch_gather_rows(const Shape& s, const void* x, const int32_t* src
 
 cudaError_t launch_group_schedule(const Shape& s, const int32_t* offsets, void* sched,
                                   int32_t* status, cudaStream_t st);
-// The float32 MLP (two kernels); mid_event (nullable) is recorded between them.
+// The float32 MLP (two kernels); mid_event (nullable) is recorded between them. src_token
+// (nullable): routed rows are read from x through it instead of from x_perm.
 cudaError_t launch_ffn_fma(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
                            const void* w_up, const void* w_down, const void* sched, void* h, void* y,
-                           cudaStream_t st, cudaEvent_t mid_event);
+                           cudaStream_t st, cudaEvent_t mid_event, const int32_t* src_token = nullptr);
 
 // A timing event: recorded as an external event node when the stream is being captured
 // into a CUDA graph, so that replays record it (a plain record would only order nodes).

@@ -182,7 +182,8 @@ cudaError_t run_router(const Shape& s, const void* x, const void* w_router, cons
 // scales (the shared expert's tokens after row R) instead of the bf16 copy in x_perm.
 cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32_t* idx, const void* x,
                         int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_token, void* x_perm,
-                        bool with_schedule, cudaStream_t st, uint8_t* x8 = nullptr, float* x8s = nullptr) {
+                        bool with_schedule, cudaStream_t st, uint8_t* x8 = nullptr, float* x8s = nullptr,
+                        bool copy_rows = true) {
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
   cudaError_t e;
@@ -200,6 +201,7 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
   if (x8 != nullptr)   // per-token codes (multi-chunk batches) go to the y region, free until the down projection
     return launch_gather_quant_rows(s, x, src_token, offsets, x8, x8s, at<uint8_t>(ws, L.y),
                                     at<float>(ws, L.xq_scale), st);
+  if (!copy_rows) return cudaSuccess;
   return launch_gather_rows(s, x, src_token, offsets, x_perm, st);
 }
 
@@ -242,8 +244,10 @@ struct ExpertWeights {
   bool a8 = false;       // W8A8: the activations entering each contraction quantised to E4M3 too
 };
 
+// src_token (nullable, float32 layers): the routed rows are read from x through it, x_perm unused.
 cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_perm, const void* x,
-                    const ExpertWeights& w, void* y, cudaStream_t st, cudaEvent_t mid_event) {
+                    const ExpertWeights& w, void* y, cudaStream_t st, cudaEvent_t mid_event,
+                    const int32_t* src_token = nullptr) {
   int32_t* status = at<int32_t>(ws, L.status);
   void* sched = at<void>(ws, L.sched);
   void* h = at<void>(ws, L.h);
@@ -265,7 +269,7 @@ cudaError_t run_ffn(const Shape& s, const WsLayout& L, void* ws, const void* x_p
     if (mid_event && (e = record_event(mid_event, st)) != cudaSuccess) return e;
     return launch_gemm_down_tc(s, h, w.d, sched, y, status, st);
   }
-  return launch_ffn_fma(s, x_perm, x, w.g, w.u, w.d, sched, h, y, st, mid_event);
+  return launch_ffn_fma(s, x_perm, x, w.g, w.u, w.d, sched, h, y, st, mid_event, src_token);
 }
 
 // FP8 weights: bf16 layers whose shapes the FP8 kernels take, aligned codes and scales.
@@ -298,6 +302,7 @@ int layer_launches(const Shape& s, int weights) {
   // code-row copy); one CTA for the first three when the batch is a single chunk of tokens
   int grouping = s.nchunks == 1 ? 2 : 4;
   if (weights == 2 && s.nchunks != 1) grouping += 1;
+  if (s.dtype == MOE_F32) grouping -= 1;                              // no grouped copy of x
   int mlp = 2;
   ExpertWeights w{nullptr, nullptr, nullptr};
   w.fp8 = weights != 0;
@@ -350,7 +355,9 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
     // W8A8: the grouped x rows go straight to E4M3 codes in the x_perm region
     uint8_t* x8 = w.a8 ? at<uint8_t>(ws, L.x_perm) : nullptr;
     float* x8s = w.a8 ? at<float>(ws, L.a8_scale) : nullptr;
-    if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st, x8, x8s) !=
+    // float32 layers: the MLP reads the routed rows from x through src_token, no grouped copy
+    const bool f32 = s.dtype == MOE_F32;
+    if (run_permute(s, L, ws, idx, x, counts, offsets, dest_row, src_token, x_perm, true, st, x8, x8s, !f32) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
   }
@@ -396,7 +403,8 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
       if (cudaMemsetAsync(acc, 0, (size_t)s.T * s.d * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
       if (launch_gemm_down_combine_tc(s, h, w.d, sched, src_token, dest_row, gate, acc, status, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    } else if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3]) != cudaSuccess) {
+    } else if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3], s.dtype == MOE_F32 ? src_token : nullptr) !=
+               cudaSuccess) {
       return MOE_ERR_CUDA;
     }
   }

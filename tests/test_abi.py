@@ -180,3 +180,13 @@ def test_launch_count_follows_the_grouping_path(monkeypatch):
     assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 2 + 1 + 1
     assert moe.moe_layer_launch_count_weights(_cfg(T=129), "w8a8") == 1 + 5 + 1 + 1
 
+
+
+def test_float32_layers_read_routed_rows_through_src_token(monkeypatch):
+    # a float32 layer's expert MLP reads x through src_token: no grouped copy of x in its
+    # permute stage (router, grouping, two MLP kernels, combine)
+    monkeypatch.delenv("MOE_FUSED_MLP", raising=False)
+    tiny = dict(d_model=64, n_experts=8, top_k=2, d_ff=128, n_shared=0, score="softmax", capacity_factor=0.0,
+                dtype="f32")
+    assert moe.moe_layer_launch_count(_cfg(T=64, **tiny)) == 1 + 1 + 2 + 1
+    assert moe.moe_layer_launch_count(_cfg(T=129, **tiny)) == 1 + 3 + 2 + 1
