@@ -151,8 +151,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, const
  *           repeated within a token) is recorded here with an atomic compare-and-swap from 0,
  *           so zero it before the call. With status == NULL such problems go unreported: the
  *           pair is still skipped (dest_row = -1) but nothing records that it happened.
- * Batches of at most 128 tokens are grouped by one CTA in its own shared memory and touch no
- * shared state. Larger batches keep the per-chunk expert histogram in a fixed 256 KiB array in
+ * Batches of at most 128 tokens are grouped in the shared memory of each block of one launch
+ * (which also copies the rows) and touch no shared state. Larger batches keep the per-chunk expert histogram in a fixed 256 KiB array in
  * libmoe.so's own device memory, held by every GPU that loads the library until the process
  * exits. It fits ceil(T/128) * E <= 65536 (T <= 32768 at E = 256); larger configurations
  * return MOE_ERR_WORKSPACE before anything is enqueued. Nothing is allocated or freed. The

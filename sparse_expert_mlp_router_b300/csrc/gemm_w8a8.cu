@@ -26,6 +26,7 @@
 #include "epilogue.cuh"
 #include "fp8_quant.cuh"
 #include "gemm_common.cuh"
+#include "group_single.cuh"
 #include "internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -329,22 +330,28 @@ __global__ void quantize_fp8_rows_kernel_act(const __nv_bfloat16* __restrict__ w
     quantize_row_e4m3_warp(w + r * cols, cols, wq + r * cols, scale + r, lane);
 }
 
-// The grouped rows of x straight to E4M3 (the W8A8 layer's grouping writes no bf16 copy):
-// row r < offsets[E] of the output is token src_token[r] quantised, and with a shared expert
-// rows R .. R+T-1 are the tokens in order. One warp per row.
-__global__ void gather_quant_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ src_token,
-                                         const int32_t* __restrict__ offsets, int E, int64_t R, int64_t n_shared_rows,
-                                         int d, uint8_t* __restrict__ dst, float* __restrict__ scale) {
+// One chunk of tokens: the grouping (every block in its own shared memory, block 0 writing it
+// out) and the grouped rows quantised as they are copied, one warp per row; the shared expert's
+// rows R .. R+T-1 are the tokens in order.
+__global__ void __launch_bounds__(kSingleThreads)
+group_quant_single_chunk_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int cap,
+                                int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                int32_t* __restrict__ dest_row, int32_t* __restrict__ src_token,
+                                int32_t* __restrict__ sched, int S, int64_t R, int32_t* status,
+                                const __nv_bfloat16* __restrict__ x, int d, uint8_t* __restrict__ dst,
+                                float* __restrict__ scale) {
+  __shared__ SingleChunkSmem sm;
+  single_chunk_group(idx, T, k, E, cap, blockIdx.x == 0, counts, offsets, dest_row, src_token, sched, S, R, status,
+                     sm);
   const int lane = threadIdx.x & 31;
-  int64_t n = offsets[E];
-  if (n > R) n = R;
-  const int64_t total = R + n_shared_rows;
+  const int64_t n = min((int64_t)sm.off[E], R);
+  const int64_t total = R + (int64_t)S * T;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t v = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); v < total; v += warps) {
     int64_t t;
     if (v < R) {
       if (v >= n) continue;
-      t = src_token[v];
+      t = sm.src[v];
     } else {
       t = v - R;
     }
@@ -415,9 +422,24 @@ cudaError_t launch_quantize_act_rows(const Shape& s, const void* src_a, const in
   return cudaGetLastError();
 }
 
-// One chunk of tokens (decode): quantise each grouped row as it is copied (one launch). Larger
-// batches, where every token appears k times among the grouped rows: quantise the T tokens once
-// into xq (codes, T x d bytes) and xq_scale, then copy code rows (half the bytes of bf16 rows).
+cudaError_t launch_group_quant_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                            int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                            const void* x, uint8_t* x8, float* x8_scale, cudaStream_t st) {
+  if (s.nchunks != 1) return cudaErrorInvalidValue;
+  const int64_t rows = s.R + (int64_t)s.S * s.T;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  int64_t blocks = (rows + 7) / 8;      // one warp per row, as the separate quantising copy
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  group_quant_single_chunk_kernel<<<(unsigned)blocks, kSingleThreads, 0, st>>>(
+      idx, s.T, s.k, s.E, s.cap, counts, offsets, dest_row, src_token, static_cast<int32_t*>(sched), s.S, s.R, status,
+      static_cast<const __nv_bfloat16*>(x), s.d, x8, x8_scale);
+  return cudaGetLastError();
+}
+
+// Batches of more than one chunk, where every token appears k times among the grouped rows:
+// quantise the T tokens once into xq (codes, T x d bytes) and xq_scale, then copy code rows
+// (half the bytes of bf16 rows). A single chunk takes launch_group_quant_single_chunk.
 cudaError_t launch_gather_quant_rows(const Shape& s, const void* x, const int32_t* src_token, const int32_t* offsets,
                                      uint8_t* x8, float* x8_scale, uint8_t* xq, float* xq_scale, cudaStream_t st) {
   const int64_t n_sh = (int64_t)s.S * s.T;
@@ -426,11 +448,7 @@ cudaError_t launch_gather_quant_rows(const Shape& s, const void* x, const int32_
   int64_t blocks = (rows + 7) / 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (s.nchunks == 1) {
-    gather_quant_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), src_token,
-                                                               offsets, s.E, s.R, n_sh, s.d, x8, x8_scale);
-    return cudaGetLastError();
-  }
+  if (s.nchunks == 1) return cudaErrorInvalidValue;
   int64_t qblocks = ((int64_t)s.T + 7) / 8;
   if (qblocks > cap) qblocks = cap;
   quantize_fp8_rows_kernel_act<<<(unsigned)qblocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), s.T, s.d,

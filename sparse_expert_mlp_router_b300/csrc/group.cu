@@ -14,6 +14,7 @@
 // expert owns a 128-bit membership mask built with atomicOr (order-free), so a
 // pair's rank inside the chunk is a popcount of the mask bits below its token;
 // a per-expert prefix over chunks then gives the global rank.
+#include "group_single.cuh"
 #include "internal.cuh"
 #include "sched.cuh"
 
@@ -156,62 +157,47 @@ __global__ void group_scatter_kernel(const int32_t* __restrict__ idx, int T, int
 // The three steps above in one CTA when the batch is a single chunk (T <= 128, decode): the
 // chunk's masks once, per-expert counts, capacity clamp and scan, the group schedule, then
 // the scatter, with the same ranks as the three-kernel path (chunk base 0).
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kSingleThreads)
 group_single_chunk_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int cap,
                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                           int32_t* __restrict__ dest_row, int32_t* __restrict__ src_token,
                           int32_t* __restrict__ sched, int S, int64_t R, int32_t* status) {
-  __shared__ uint32_t mask[kMaxExperts * kWords];
-  __shared__ bool dup[kChunk * kMaxTopK];
-  __shared__ int32_t warp_tot[kScanThreads / 32];
-  __shared__ int32_t s_off[kMaxExperts + 1];
-  build_masks(mask, idx, 0, T, k, E, status, dup);
-  const int e = threadIdx.x;
-  int n = 0;
-  if (e < E) {
-#pragma unroll
-    for (int w = 0; w < kWords; ++w) n += __popc(mask[e * kWords + w]);
-    counts[e] = n;
+  __shared__ SingleChunkSmem sm;
+  single_chunk_group(idx, T, k, E, cap, true, counts, offsets, dest_row, src_token, sched, S, R, status, sm);
+}
+
+// One warp copies grouped row r = token t's row of x: 16-byte vectors, four loads in flight per
+// lane before their stores.
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ x, int64_t t, uint4* __restrict__ dst,
+                                         int vec_per_row, int lane) {
+  const uint4* src = x + (size_t)t * vec_per_row;
+  int v = lane;
+  for (; v + 96 < vec_per_row; v += 128) {
+    const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), e = __ldg(src + v + 96);
+    dst[v] = a;
+    dst[v + 32] = b;
+    dst[v + 64] = c;
+    dst[v + 96] = e;
   }
-  const int kv = (e < E) ? min(n, cap) : 0;
-  const int lane = e & 31, warp = e >> 5;
-  int incl = kv;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int w = 0; w < warp; ++w) base += warp_tot[w];
-  if (e < E) {
-    offsets[e] = base + incl - kv;
-    s_off[e] = base + incl - kv;
-  }
-  if (e == kScanThreads - 1) {
-    offsets[E] = base + incl;
-    s_off[E] = base + incl;
-  }
-  __syncthreads();
-  if (sched != nullptr && warp == 0) build_schedule_warp(s_off, false, E, S, T, R, sched);
-  for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
-    const int t = p / k;
-    const int ex = idx[p];
-    int row = -1;
-    if (!dup[p]) {
-      const uint32_t* m = mask + ex * kWords;
-      int r = 0;
-      for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
-      r += __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
-      const int lo = s_off[ex], hi = s_off[ex + 1];
-      if (r < hi - lo) {
-        row = lo + r;
-        src_token[row] = t;
-      }
-    }
-    dest_row[p] = row;
-  }
+  for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+}
+
+// The single-chunk grouping and the grouped copy of x in one launch: every block rebuilds the
+// grouping in shared memory (block 0 writes it out), then copies its rows, one warp per row.
+__global__ void __launch_bounds__(kSingleThreads)
+group_gather_single_chunk_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int cap,
+                                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                 int32_t* __restrict__ dest_row, int32_t* __restrict__ src_token,
+                                 int32_t* __restrict__ sched, int S, int64_t R, int32_t* status,
+                                 const uint4* __restrict__ x, int vec_per_row, uint4* __restrict__ x_perm) {
+  __shared__ SingleChunkSmem sm;
+  single_chunk_group(idx, T, k, E, cap, blockIdx.x == 0, counts, offsets, dest_row, src_token, sched, S, R, status,
+                     sm);
+  const int64_t n_rows = min((int64_t)sm.off[E], R);
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows; r += warps)
+    copy_row(x, sm.src[r], x_perm + (size_t)r * vec_per_row, vec_per_row, lane);
 }
 
 // x_perm[r] = x[src_token[r]] for r < offsets[E]; one warp per row, 16-byte vectors.
@@ -221,21 +207,8 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
   const int64_t n_rows = min((int64_t)offsets[E], R);
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows; r += warps) {
-    const int t = src_token[r];
-    const uint4* src = x + (size_t)t * vec_per_row;
-    uint4* dst = x_perm + (size_t)r * vec_per_row;
-    // four 16-byte loads in flight per lane before their stores
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), e = __ldg(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = e;
-    }
-    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
-  }
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows; r += warps)
+    copy_row(x, src_token[r], x_perm + (size_t)r * vec_per_row, vec_per_row, lane);
 }
 
 }  // namespace
@@ -264,7 +237,7 @@ cudaError_t launch_group_single_chunk(const Shape& s, const int32_t* idx, int32_
                                       int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
                                       cudaStream_t st) {
   if (s.nchunks != 1) return cudaErrorInvalidValue;
-  group_single_chunk_kernel<<<1, kScanThreads, 0, st>>>(idx, s.T, s.k, s.E, s.cap, counts, offsets, dest_row,
+  group_single_chunk_kernel<<<1, kSingleThreads, 0, st>>>(idx, s.T, s.k, s.E, s.cap, counts, offsets, dest_row,
                                                         src_token, static_cast<int32_t*>(sched), s.S, s.R, status);
   return cudaGetLastError();
 }
@@ -279,6 +252,21 @@ cudaError_t launch_gather_rows(const Shape& s, const void* x, const int32_t* src
   if (blocks < 1) blocks = 1;
   gather_rows_kernel<<<(unsigned)blocks, threads, 0, st>>>(static_cast<const uint4*>(x), src_token, offsets, s.E,
                                                             vec_per_row, s.R, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_gather_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                             int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                             const void* x, void* x_perm, cudaStream_t st) {
+  if (s.nchunks != 1) return cudaErrorInvalidValue;
+  const int vec_per_row = (int)((size_t)s.d * s.esize / 16);
+  int64_t blocks = (s.R + 7) / 8;       // one warp per row, as the separate copy
+  const int64_t cap = (int64_t)num_sms() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  group_gather_single_chunk_kernel<<<(unsigned)blocks, kSingleThreads, 0, st>>>(
+      idx, s.T, s.k, s.E, s.cap, counts, offsets, dest_row, src_token, static_cast<int32_t*>(sched), s.S, s.R, status,
+      static_cast<const uint4*>(x), vec_per_row, static_cast<uint4*>(x_perm));
   return cudaGetLastError();
 }
 

@@ -105,6 +105,11 @@ cudaError_t launch_group_single_chunk(const Shape& s, const int32_t* idx, int32_
                                       cudaStream_t st);
 cudaError_t launch_gather_rows(const Shape& s, const void* x, const int32_t* src_token,
                                const int32_t* offsets, void* x_perm, cudaStream_t st);
+// The single-chunk grouping and the grouped copy of x in one launch (every block groups in its
+// own shared memory, block 0 writes the grouping out, each block copies its rows).
+cudaError_t launch_group_gather_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                             int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                             const void* x, void* x_perm, cudaStream_t st);
 
 cudaError_t launch_group_schedule(const Shape& s, const int32_t* offsets, void* sched,
                                   int32_t* status, cudaStream_t st);
@@ -169,10 +174,15 @@ cudaError_t launch_quantize_act_rows(const Shape& s, const void* src_a, const in
                                      const void* src_b, int64_t n_b, int cols, uint8_t* dst, float* scale,
                                      cudaStream_t st);
 // x rows of the grouping (src_token order; the shared expert's tokens after row R) -> E4M3
-// codes and per-row scales, in place of the bf16 row copy. xq [T, d] bytes and xq_scale [T]:
-// scratch for the per-token codes of multi-chunk batches.
+// codes and per-row scales, in place of the bf16 row copy, for batches of more than one chunk.
+// xq [T, d] bytes and xq_scale [T]: scratch for the per-token codes.
 cudaError_t launch_gather_quant_rows(const Shape& s, const void* x, const int32_t* src_token, const int32_t* offsets,
                                      uint8_t* x8, float* x8_scale, uint8_t* xq, float* xq_scale, cudaStream_t st);
+// W8A8, a single chunk: the grouping and the grouped rows as E4M3 codes in one launch (as
+// launch_group_gather_single_chunk, each block quantising its rows; the shared expert's after R).
+cudaError_t launch_group_quant_single_chunk(const Shape& s, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                            int32_t* dest_row, int32_t* src_token, void* sched, int32_t* status,
+                                            const void* x, uint8_t* x8, float* x8_scale, cudaStream_t st);
 cudaError_t launch_gemm_gateup_w8a8(const Shape& s, const uint8_t* x8, const float* x8_scale, const uint8_t* wg_q,
                                     const float* wg_s, const uint8_t* wu_q, const float* wu_s, const void* sched,
                                     void* h, int32_t* status, cudaStream_t st);

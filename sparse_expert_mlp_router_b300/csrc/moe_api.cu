@@ -187,10 +187,17 @@ cudaError_t run_permute(const Shape& s, const WsLayout& L, void* ws, const int32
   int32_t* status = at<int32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
   cudaError_t e;
-  if (s.nchunks == 1) {       // one chunk of tokens (decode): the three grouping steps in one CTA
-    if ((e = launch_group_single_chunk(s, idx, counts, offsets, dest_row, src_token,
-                                       with_schedule ? at<void>(ws, L.sched) : nullptr, status, st)) != cudaSuccess)
-      return e;
+  if (s.nchunks == 1) {
+    // one chunk of tokens (decode): the three grouping steps and the row copy (or quantising
+    // copy) in one launch, each block grouping in its own shared memory
+    void* sched = with_schedule ? at<void>(ws, L.sched) : nullptr;
+    if (x8 != nullptr)
+      return launch_group_quant_single_chunk(s, idx, counts, offsets, dest_row, src_token, sched, status, x, x8, x8s,
+                                             st);
+    if (copy_rows)
+      return launch_group_gather_single_chunk(s, idx, counts, offsets, dest_row, src_token, sched, status, x, x_perm,
+                                              st);
+    return launch_group_single_chunk(s, idx, counts, offsets, dest_row, src_token, sched, status, st);
   } else {
     if ((e = launch_group_hist(s, idx, cc, status, st)) != cudaSuccess) return e;
     if ((e = launch_group_scan(s, cc, counts, offsets, with_schedule ? at<void>(ws, L.sched) : nullptr, st)) !=
@@ -299,10 +306,10 @@ bool fused_combine(const Shape& s, const ExpertWeights& w) {
 // activations, 2 W8A8. Memset nodes are not counted.
 int layer_launches(const Shape& s, int weights) {
   // grouping: hist, scan (+ group schedule), scatter, row copy (W8A8: per-token quantiser and
-  // code-row copy); one CTA for the first three when the batch is a single chunk of tokens
-  int grouping = s.nchunks == 1 ? 2 : 4;
+  // code-row copy); one launch of all of it when the batch is a single chunk of tokens
+  int grouping = s.nchunks == 1 ? 1 : 4;
   if (weights == 2 && s.nchunks != 1) grouping += 1;
-  if (s.dtype == MOE_F32) grouping -= 1;                              // no grouped copy of x
+  if (s.dtype == MOE_F32 && s.nchunks != 1) grouping -= 1;            // no grouped copy of x
   int mlp = 2;
   ExpertWeights w{nullptr, nullptr, nullptr};
   w.fp8 = weights != 0;

@@ -12,8 +12,9 @@
 //
 // Limits and sharing:
 //   * a batch of at most 128 tokens (one chunk: decode-sized batches) is grouped
-//     by a single CTA that keeps its histogram in shared memory; such calls never
-//     touch the array below and cannot race with other calls;
+//     in one launch whose blocks each keep the histogram in their own shared
+//     memory; such calls never touch the array below and cannot race with other
+//     calls;
 //   * larger batches use the array: kNoAllocScratchInts int32 (256 KiB); a
 //     configuration needs ceil(T/128) * E of them, so e.g. T <= 32768 at E = 256
 //     or T <= 65536 at E = 128. Larger configurations are refused with
@@ -118,11 +119,11 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32
     return MOE_ERR_INVALID_ARG;
   const Shape s = make_shape(*cfg);
   if (s.nchunks == 1) {
-    // one chunk of tokens: histogram, scan and scatter in one CTA's shared memory
-    if (launch_group_single_chunk(s, topk_idx, counts, offsets, dest_row, src_token, nullptr, status, stream) !=
-        cudaSuccess)
+    // one chunk of tokens: histogram, scan, scatter and the row copy in one launch, each block
+    // grouping in its own shared memory
+    if (launch_group_gather_single_chunk(s, topk_idx, counts, offsets, dest_row, src_token, nullptr, status, x,
+                                         x_perm, stream) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_gather_rows(s, x, src_token, offsets, x_perm, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
   if ((int64_t)s.nchunks * s.E > kNoAllocScratchInts) return MOE_ERR_WORKSPACE;

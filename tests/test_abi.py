@@ -144,12 +144,12 @@ def test_fp8_quantiser_and_stats_validation_before_any_launch():
 
 
 def test_launch_count_follows_the_grouping_path(monkeypatch):
-    # router, grouping (one kernel for a single 128-token chunk, else histogram, scan and
-    # scatter), the row copy, the expert MLP (one persistent launch of both contractions for a
-    # single chunk of a bf16 layer, else two) and the combine
+    # router, grouping (one kernel with the row copy for a single 128-token chunk, else
+    # histogram, scan, scatter and the row copy), the expert MLP (one persistent launch of both
+    # contractions for a single chunk of a bf16 layer, else two) and the combine
     monkeypatch.delenv("MOE_FUSED_MLP", raising=False)
     assert moe.moe_layer_mlp_fused(_cfg(T=128)) == 1
-    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 1 + 1
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 1 + 1 + 1
     assert moe.moe_layer_mlp_fused(_cfg(T=129)) == 0
     assert moe.moe_layer_launch_count(_cfg(T=129)) == 1 + 4 + 2 + 1
     assert moe.moe_layer_launch_count(_cfg(top_k=300)) == -1
@@ -157,16 +157,16 @@ def test_launch_count_follows_the_grouping_path(monkeypatch):
     # the environment forces either way (read at every call); float32 layers always take two
     monkeypatch.setenv("MOE_FUSED_MLP", "0")
     assert moe.moe_layer_mlp_fused(_cfg(T=128)) == 0
-    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 2 + 2 + 1
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 1 + 2 + 1
     monkeypatch.setenv("MOE_FUSED_MLP", "1")
     assert moe.moe_layer_mlp_fused(_cfg(T=129)) == 1
     assert moe.moe_layer_mlp_fused(_cfg(T=128, dtype="f32")) == 0
     # per weight format: FP8 weights keep two expert launches; W8A8 three (gate/up, h's
     # quantiser, down), and for multi-chunk batches a per-token quantiser before the code-row copy
     monkeypatch.delenv("MOE_FUSED_MLP", raising=False)
-    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "bf16") == 1 + 2 + 1 + 1
-    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "fp8") == 1 + 2 + 2 + 1
-    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 2 + 3 + 1
+    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "bf16") == 1 + 1 + 1 + 1
+    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "fp8") == 1 + 1 + 2 + 1
+    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 1 + 3 + 1
     assert moe.moe_layer_mlp_fused_weights(_cfg(T=128), "bf16") == 1
     assert moe.moe_layer_mlp_fused_weights(_cfg(T=128), "fp8") == 0
     assert moe.moe_layer_mlp_fused_weights(_cfg(T=128), "w8a8") == 0
@@ -177,7 +177,7 @@ def test_launch_count_follows_the_grouping_path(monkeypatch):
     # W8A8 as one launch only on request (it measured slower than three)
     monkeypatch.setenv("MOE_FUSED_MLP", "1")
     assert moe.moe_layer_mlp_fused_weights(_cfg(T=128), "w8a8") == 1
-    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 2 + 1 + 1
+    assert moe.moe_layer_launch_count_weights(_cfg(T=128), "w8a8") == 1 + 1 + 1 + 1
     assert moe.moe_layer_launch_count_weights(_cfg(T=129), "w8a8") == 1 + 5 + 1 + 1
 
 
