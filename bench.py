@@ -738,7 +738,9 @@ def measure_workload(args, w, dist, local, rank, world, with_cpu: bool, weights:
             roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
         roof["kernel"] = ("grouped_mlp_w8a8_fused_kernel<gate/up + SwiGLU, h to E4M3, then down, one launch> "
                           "(tcgen05 kind::f8f6f4)" if one_mlp and a8 else
-                          "grouped_mlp_fused_kernel<gate/up + SwiGLU, then down, one launch> (tcgen05)" if one_mlp else
+                          ("grouped_mlp_fused_kernel<gate/up + SwiGLU, then down and the combine, one launch> (tcgen05)"
+                           if os.environ.get("MOE_MLP_COMBINE") == "1" else
+                           "grouped_mlp_fused_kernel<gate/up + SwiGLU, then down, one launch> (tcgen05)") if one_mlp else
                           "grouped_gemm_w8a8_kernel<gate/up, E4M3 weights and activations, SwiGLU epilogue> "
                           "(tcgen05 kind::f8f6f4)" if a8 else
                           "grouped_gemm_fp8w_kernel<gate/up, FP8 weights, SwiGLU epilogue> (tcgen05)" if fp8 else

@@ -17,6 +17,14 @@
 // M=128, N=256, two TMEM accumulators), warps 2-9 epilogue (staged whole-sector stores). h is
 // written by generic stores and read by TMA in other CTAs: the writers fence the generic proxy
 // against the async proxy before publishing, the reader fences again after acquiring.
+//
+// With COMBINE the down tiles also produce the layer output (the deterministic gather-reduce
+// of the combine, klaylearn.com/glossary/mixture-of-experts: restore token order): once a down
+// tile's rows are stored, one thread per row fences and adds one (acquire-release) to its
+// token's counter; the add that reaches the token's total (down n-tiles x its kept rows and
+// shared row) queues the token, and the tile's 256 epilogue threads sum its rows in slot order
+// with the separate combine kernel's arithmetic, so the output has the same bits. No thread
+// waits for another: the last arrival does the work.
 #include "epilogue.cuh"
 #include "gemm_common.cuh"
 #include "internal.cuh"
@@ -42,7 +50,9 @@ constexpr int kStages = 4;
 constexpr int kTmemCols = 512;
 constexpr int kSchedInts = 4 * (kMaxExperts + 2);
 constexpr size_t kStgOff = (size_t)kStages * kStageBytes + 256 + (((size_t)kSchedInts * 4 + 127) / 128) * 128;
-constexpr size_t kSmem = 1024 + kStgOff + (size_t)kEpiWarps * epi::kStageOutBytes;
+constexpr size_t kListOff = kStgOff + (size_t)kEpiWarps * epi::kStageOutBytes;
+constexpr size_t kSmem = 1024 + kListOff + (size_t)kBM * 4;     // + the tokens a down tile completes
+constexpr int kEpiThreads = 32 * kEpiWarps;
 
 struct FusedArgs {
   int K1, K2;             // reductions: d (gate/up), d_ff (down)
@@ -54,6 +64,15 @@ struct FusedArgs {
   __nv_bfloat16* y;       // [rows, d]
   int32_t* ready;         // [m-tiles]: published epilogue-warp counts of finished gate/up tiles
   int32_t* status;
+  // the combine in the down tiles (COMBINE): out[t] = sum over t's kept slots j in slot order of
+  // gate[t, j] * y[dest_row[t, j]] (+ y[R + t] with a shared expert), by the tile that completes t
+  const int32_t* src_token;
+  const int32_t* dest_row;
+  const float* gate;
+  __nv_bfloat16* out;
+  int32_t* tok_done;      // [T]: finished (row, down n-tile) pieces of each token
+  int k, T, S;
+  int64_t R;
 };
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -66,6 +85,68 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ int atom_acq_rel_add(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+// the eight epilogue warps (threads 64 .. 319)
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory"); }
+
+// Rows of token t the down tiles write: its kept slots (dest_row in [0, R)) and the shared
+// expert's row.
+__device__ __forceinline__ int token_rows(const FusedArgs& a, int t) {
+  int n = a.S;
+  for (int j = 0; j < a.k; ++j) {
+    const int r = __ldg(a.dest_row + (int64_t)t * a.k + j);
+    n += (r >= 0 && r < a.R) ? 1 : 0;
+  }
+  return n;
+}
+
+// Token t's output row by the 256 epilogue threads (et = 0 .. 255), 8 columns per thread and
+// pass: the arithmetic of the separate combine kernel (float32, slot order, the shared row
+// last), so the same bits. y rows were written by other CTAs in this launch: coherent loads.
+__device__ __forceinline__ void combine_token(const FusedArgs& a, int t, int et) {
+  for (int c = et * 8; c < a.d; c += kEpiThreads * 8) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+      int r = __ldg(a.dest_row + (int64_t)t * a.k + j);
+      if (r >= a.R) {
+        set_status(a.status, MOE_ERR_DEVICE_INDEX);
+        r = -1;
+      }
+      if (r < 0) continue;
+      const uint4 u = __ldcg(reinterpret_cast<const uint4*>(a.y + (int64_t)r * a.d + c));
+      const float g = __ldg(a.gate + (int64_t)t * a.k + j);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(g, __uint_as_float(w[i] << 16), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g, __uint_as_float(w[i] & 0xFFFF0000u), acc[2 * i + 1]);
+      }
+    }
+    if (a.S > 0) {
+      const uint4 u = __ldcg(reinterpret_cast<const uint4*>(a.y + (a.R + t) * a.d + c));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += __uint_as_float(w[i] << 16);
+        acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(a.out + (int64_t)t * a.d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // Wait until *p >= target, giving up after limit_ns or when *abort is set. True on success.
@@ -83,6 +164,7 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatil
   }
 }
 
+template <bool COMBINE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXs,
                          const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ CUtensorMap tmWu,
@@ -100,6 +182,9 @@ grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
   uint64_t* drain = tempty + 2;                // [1]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* s_stop = abort_flag + 1;       // COMBINE: the epilogue's snapshot of the abort flag
+  int* s_ncomb = const_cast<int*>(abort_flag + 2);   // COMBINE: tokens the current down tile completed
+  int32_t* s_list = reinterpret_cast<int32_t*>(smem + kListOff);
   int32_t* s_tile_start = reinterpret_cast<int32_t*>(smem + (size_t)kStages * kStageBytes + 256);
   int32_t* s_a_row = s_tile_start + (args.G + 1);
   int32_t* s_out_row = s_a_row + args.G;
@@ -252,7 +337,15 @@ grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
+    const int et = threadIdx.x - 64;                 // 0 .. 255
     const uint32_t stg = stg_base + (uint32_t)(warp - 2) * epi::kStageOutBytes;
+    if constexpr (COMBINE) {
+      // tokens no row reaches (every slot dropped, no shared expert) get a zero output row here
+      for (int t = (int)blockIdx.x * kEpiThreads + et; t < args.T; t += (int)gridDim.x * kEpiThreads)
+        if (token_rows(args, t) == 0)
+          for (int c = 0; c < args.d; c += 8)
+            *reinterpret_cast<uint4*>(args.out + (int64_t)t * args.d + c) = make_uint4(0, 0, 0, 0);
+    }
     int it = 0;
     for (int L = blockIdx.x; L < total; L += gridDim.x, ++it) {
       const bool up = L < n1;
@@ -263,7 +356,14 @@ grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
       if (!ptx::mbar_wait_bounded(ptx::smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs)) {
         set_status(args.status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
-        break;
+        if (!COMBINE) break;
+      }
+      if constexpr (COMBINE) {
+        // the epilogue warps meet at named barriers: all eight leave on the same snapshot
+        epi_bar();
+        if (et == 0) *s_stop = *abort_flag;
+        epi_bar();
+        if (*s_stop != 0) break;
       }
       ptx::tc_fence_after();
       const int row0 = m * kBM + quarter * 32;
@@ -281,8 +381,29 @@ grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         epi::store_tile<false, 256>(t_row, s_rows[g] - row0, args.y + orow * args.d + (int64_t)n * 256, args.d, half,
                                     stg, lane);
       }
+      // the accumulator is free: the combine below reads y, not TMEM
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_u32(&tempty[acc]));
+      if (!up) {
+        if constexpr (COMBINE) {
+          // count this tile's rows on their tokens: the barrier orders all eight warps' stores
+          // before each counting thread's gpu-scope release; the count that completes a token
+          // queues it, and the warps combine it
+          if (et == 0) *s_ncomb = 0;
+          epi_bar();
+          const int rows_here = min(kBM, s_rows[g] - m * kBM);
+          if (et < rows_here) {
+            const int lr = m * kBM + et;
+            const int t = (g >= args.E) ? lr : __ldg(args.src_token + s_out_row[g] + lr);
+            const int target = token_rows(args, t) * args.nt2;
+            if (atom_acq_rel_add(args.tok_done + t, 1) + 1 == target) s_list[atomicAdd(s_ncomb, 1)] = t;
+          }
+          epi_bar();
+          const int nc = *s_ncomb;
+          for (int i = 0; i < nc; ++i) combine_token(args, s_list[i], et);
+          epi_bar();
+        }
+      }
     }
   }
 
@@ -302,11 +423,12 @@ int64_t max_m_tiles(const Shape& s) {
 
 bool fused_mlp_supported(const Shape& s) { return s.dtype == MOE_BF16 && s.d % 256 == 0 && s.F % 128 == 0; }
 
-int64_t fused_mlp_ready_ints(const Shape& s) { return max_m_tiles(s); }
+int64_t fused_mlp_ready_ints(const Shape& s) { return max_m_tiles(s) + s.T; }
 
 cudaError_t launch_mlp_fused_tc(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
                                 const void* w_up, const void* w_down, const void* sched, void* h, void* y,
-                                int32_t* ready, int32_t* status, cudaStream_t st) {
+                                int32_t* ready, int32_t* status, cudaStream_t st, const int32_t* src_token,
+                                const int32_t* dest_row, const float* gate, void* out) {
   CUtensorMap tx, txs, twg, twu, th, twd;
   const uint64_t R = (uint64_t)(s.R > 0 ? s.R : 1);
   const uint64_t rows = (uint64_t)s.R + (uint64_t)s.S * s.T;
@@ -330,15 +452,27 @@ cudaError_t launch_mlp_fused_tc(const Shape& s, const void* x_perm, const void* 
   args.y = static_cast<__nv_bfloat16*>(y);
   args.ready = ready;
   args.status = status;
-  cudaError_t e = cudaMemsetAsync(ready, 0, (size_t)max_m_tiles(s) * sizeof(int32_t), st);
+  const bool combine = out != nullptr;
+  if (combine && (src_token == nullptr || dest_row == nullptr || gate == nullptr)) return cudaErrorInvalidValue;
+  args.src_token = src_token;
+  args.dest_row = dest_row;
+  args.gate = gate;
+  args.out = static_cast<__nv_bfloat16*>(out);
+  args.tok_done = ready + max_m_tiles(s);
+  args.k = s.k;
+  args.T = s.T;
+  args.S = s.S;
+  args.R = s.R;
+  cudaError_t e = cudaMemsetAsync(ready, 0, (size_t)(max_m_tiles(s) + (combine ? s.T : 0)) * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(grouped_mlp_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  auto kern = combine ? grouped_mlp_fused_kernel<true> : grouped_mlp_fused_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;
   int64_t grid = num_sms();
   const int64_t max_tiles = max_m_tiles(s) * (args.nt1 + args.nt2);
   if (max_tiles < grid) grid = max_tiles;
   if (grid < 1) grid = 1;
-  grouped_mlp_fused_kernel<<<(unsigned)grid, kThreads, kSmem, st>>>(tx, txs, twg, twu, th, twd, args);
+  kern<<<(unsigned)grid, kThreads, kSmem, st>>>(tx, txs, twg, twu, th, twd, args);
   return cudaGetLastError();
 }
 

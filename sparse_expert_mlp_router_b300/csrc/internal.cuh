@@ -152,12 +152,15 @@ cudaError_t launch_gemm_down_fp8w(const Shape& s, const void* h, const uint8_t* 
                                   const void* sched, void* y, int32_t* status, cudaStream_t st);
 
 // Both contractions of the bf16 expert MLP in one persistent launch (gemm_fused.cu); `ready`
-// holds fused_mlp_ready_ints(s) int32 (zeroed by the launcher).
+// holds fused_mlp_ready_ints(s) int32 (zeroed by the launcher). out non-NULL: the down tiles
+// also combine (each token's output row by the tile that completes it; src_token, dest_row
+// and gate of the grouping and router), with the separate combine's bits.
 bool fused_mlp_supported(const Shape& s);
 int64_t fused_mlp_ready_ints(const Shape& s);
 cudaError_t launch_mlp_fused_tc(const Shape& s, const void* x_perm, const void* x, const void* w_gate,
                                 const void* w_up, const void* w_down, const void* sched, void* h, void* y,
-                                int32_t* ready, int32_t* status, cudaStream_t st);
+                                int32_t* ready, int32_t* status, cudaStream_t st, const int32_t* src_token = nullptr,
+                                const int32_t* dest_row = nullptr, const float* gate = nullptr, void* out = nullptr);
 
 // The W8A8 expert MLP in one persistent launch (gemm_w8a8_fused.cu); `counters` holds
 // 2 * fused_mlp_ready_ints(s) int32 (zeroed by the launcher).

@@ -239,6 +239,18 @@ bool fused_mlp_w8a8(const Shape& s) {
   return v != nullptr && v[0] == '1';
 }
 
+// Whether the one-launch bf16 expert MLP also combines (each token's output row summed by the
+// down tile that completes the token, in slot order: the separate combine's bits) instead of a
+// combine launch after it: only with MOE_MLP_COMBINE=1 in the environment (read at every
+// call), since on the decode batch it measured slower (0.203 vs 0.186 ms: the per-tile barriers
+// of the epilogue warps and the per-token acquire-release counts slow the whole pipeline by
+// more than the 6.6 us combine launch it saves).
+bool mlp_combine(const Shape& s) {
+  if (!fused_mlp(s)) return false;
+  const char* v = getenv("MOE_MLP_COMBINE");
+  return v != nullptr && v[0] == '1';
+}
+
 // Expert weights of a call: bf16 / float32 tensors, or FP8 codes with per-row scales.
 struct ExpertWeights {
   const void* g;
@@ -315,7 +327,8 @@ int layer_launches(const Shape& s, int weights) {
   w.fp8 = weights != 0;
   if (weights == 2) mlp = fused_mlp_w8a8(s) ? 1 : 3;                 // + the quantiser of h
   else if (weights == 0 && s.dtype == MOE_BF16 && !fused_combine(s, w) && fused_mlp(s)) mlp = 1;
-  return 1 /*router*/ + grouping + mlp + 1 /*combine*/;
+  const int combine = (mlp == 1 && weights == 0 && mlp_combine(s)) ? 0 : 1;   // in the one-launch MLP
+  return 1 /*router*/ + grouping + mlp + combine;
 }
 
 moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w_router, const float* bias,
@@ -370,6 +383,8 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
   }
   if (!mark(2)) return MOE_ERR_CUDA;
   const bool fused = fused_combine(s, w);
+  // the one-launch bf16 MLP with the combine in its down tiles
+  const bool mlp_comb = !w.fp8 && !fused && s.dtype == MOE_BF16 && mlp_combine(s);
   float* acc = at<float>(ws, L.y);
   {
     const NvtxRange r("moe_layer/experts");
@@ -410,13 +425,19 @@ moe_status_t layer_forward(const moe_config_t* cfg, const void* x, const void* w
       if (cudaMemsetAsync(acc, 0, (size_t)s.T * s.d * sizeof(float), st) != cudaSuccess) return MOE_ERR_CUDA;
       if (launch_gemm_down_combine_tc(s, h, w.d, sched, src_token, dest_row, gate, acc, status, st) != cudaSuccess)
         return MOE_ERR_CUDA;
+    } else if (mlp_comb) {
+      // both contractions and the combine in one launch: the stage boundary events fall before it
+      if (!mark(3)) return MOE_ERR_CUDA;
+      if (launch_mlp_fused_tc(s, x_perm, x, w.g, w.u, w.d, at<void>(ws, L.sched), at<void>(ws, L.h), y,
+                              at<int32_t>(ws, L.mlp_ready), status, st, src_token, dest_row, gate, out) != cudaSuccess)
+        return MOE_ERR_CUDA;
     } else if (run_ffn(s, L, ws, x_perm, x, w, y, st, ev[3], s.dtype == MOE_F32 ? src_token : nullptr) !=
                cudaSuccess) {
       return MOE_ERR_CUDA;
     }
   }
   if (!mark(4)) return MOE_ERR_CUDA;
-  {
+  if (!mlp_comb) {
     const NvtxRange r("moe_layer/combine");
     if (fused ? launch_combine_finalize(s, acc, out, st) != cudaSuccess
               : launch_combine(s, y, dest_row, gate, out, status, st) != cudaSuccess)

@@ -148,8 +148,13 @@ def test_launch_count_follows_the_grouping_path(monkeypatch):
     # histogram, scan, scatter and the row copy), the expert MLP (one persistent launch of both
     # contractions for a single chunk of a bf16 layer, else two) and the combine
     monkeypatch.delenv("MOE_FUSED_MLP", raising=False)
+    monkeypatch.delenv("MOE_MLP_COMBINE", raising=False)
     assert moe.moe_layer_mlp_fused(_cfg(T=128)) == 1
     assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 1 + 1 + 1
+    monkeypatch.setenv("MOE_MLP_COMBINE", "1")                    # the combine inside the one launch
+    assert moe.moe_layer_launch_count(_cfg(T=128)) == 1 + 1 + 1 + 0
+    assert moe.moe_layer_launch_count(_cfg(T=129)) == 1 + 4 + 2 + 1   # two MLP launches: no effect
+    monkeypatch.delenv("MOE_MLP_COMBINE")
     assert moe.moe_layer_mlp_fused(_cfg(T=129)) == 0
     assert moe.moe_layer_launch_count(_cfg(T=129)) == 1 + 4 + 2 + 1
     assert moe.moe_layer_launch_count(_cfg(top_k=300)) == -1

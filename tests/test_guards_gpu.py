@@ -144,10 +144,14 @@ def test_w8a8_layer_writes_only_its_outputs(name, edit):
     _check_all(bufs, f"w8a8 layer {name}")
 
 
-@pytest.mark.parametrize("name,edit", [("mini_deepseek", {}), ("mini_decode", {}), ("mini_mixtral", {"T": 1200})])
-def test_fused_mlp_layer_writes_only_its_outputs(name, edit, monkeypatch):
-    # the one-launch expert MLP keeps its per-m-tile counters inside the workspace
+@pytest.mark.parametrize("combine", ["0", "1"])
+@pytest.mark.parametrize("name,edit", [("mini_deepseek", {}), ("mini_decode", {}), ("mini_mixtral", {"T": 1200}),
+                                       ("mini_qwen3", {"T": 100, "capacity_factor": 0.05})])
+def test_fused_mlp_layer_writes_only_its_outputs(name, edit, combine, monkeypatch):
+    # the one-launch expert MLP keeps its per-m-tile (and, combining, per-token) counters inside
+    # the workspace; combining, it writes the output rows itself
     monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    monkeypatch.setenv("MOE_MLP_COMBINE", combine)
     w = synth.WORKLOADS[name].with_(**edit)
     dev = Inputs(w).device()
     cfg = cfg_of(w)

@@ -252,3 +252,35 @@ def test_layer_fused_mlp_full_size_bit_identical(name, monkeypatch):
         assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     del dev
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,edit,force_one_launch", [
+    ("mini_decode", {}, False),
+    ("mini_decode", dict(T=1), False),
+    ("mini_qwen3", dict(T=128), False),                            # one full chunk
+    ("mini_qwen3", dict(T=100, capacity_factor=0.05), False),      # tokens with every slot dropped
+    ("mini_deepseek", dict(T=128), False),                         # shared expert, drops, sigmoid
+    ("mini_mixtral", dict(T=64), False),
+    ("mini_qwen3", {}, True),                                      # three chunks, one launch forced
+])
+def test_layer_mlp_combine_is_bit_identical(name, edit, force_one_launch, monkeypatch):
+    # MOE_MLP_COMBINE=1: the one-launch expert MLP combines in its down tiles: each (row, down
+    # n-tile) is counted on its token, and the tile that completes a token sums the token's rows
+    # in slot order, the arithmetic of the separate combine kernel (=0). Outputs agree bit for
+    # bit; tokens that no row reaches get zero rows
+    w = synth.WORKLOADS[name].with_(**edit)
+    inp = Inputs(w)
+    dev = inp.device()
+    cfg = cfg_of(w)
+    if force_one_launch:
+        monkeypatch.setenv("MOE_FUSED_MLP", "1")
+    monkeypatch.setenv("MOE_MLP_COMBINE", "0")
+    n_sep = moe.moe_layer_launch_count(cfg)
+    ref_out, ref_idx, _ = _run_layer(w, dev, cfg)
+    monkeypatch.setenv("MOE_MLP_COMBINE", "1")
+    assert moe.moe_layer_launch_count(cfg) == n_sep - 1
+    out, idx, _ = _run_layer(w, dev, cfg)
+    assert (idx == ref_idx).all()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    res, _ = _oracle_on_gpu_routing(w, inp.f64["x"], inp.f64["w_router"], inp.bias, inp.expert, idx)
+    assert_close(to_f64(out), res.out, out_tolerance(w), f"mlp combine {name} {edit}")
