@@ -1,6 +1,7 @@
 """Failure paths on the GPU, none of which faults or hangs it: out-of-range ids and
 corrupt offsets are skipped and recorded, a stalled wait gives up and reports a
 status, and the context stays usable afterwards."""
+import numpy as np
 import pytest
 import torch
 
@@ -30,14 +31,16 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert torch.isfinite(out.float()).all()
 
 
-def test_out_of_range_ids_are_skipped_and_flagged():
-    w = synth.WORKLOADS["mini_qwen3"]
+@pytest.mark.parametrize("T", [333, 100])             # multi-chunk kernels; one launch for a single chunk
+def test_out_of_range_ids_are_skipped_and_flagged(T):
+    w = synth.WORKLOADS["mini_qwen3"].with_(T=T)
     cfg = cfg_of(w)
     dev = Inputs(w).device()
-    idx = torch.randint(0, w.n_experts, (w.T, w.top_k), dtype=torch.int32, device="cuda")
-    idx[:, 0] = torch.arange(w.T, dtype=torch.int32, device="cuda") % w.n_experts
+    # distinct experts per token (a random permutation's first k), then the bad entries
+    idx = torch.argsort(torch.rand(w.T, w.n_experts, device="cuda"), dim=1)[:, :w.top_k].to(torch.int32)
     idx[5, 3] = w.n_experts + 3
     idx[7, 0] = -1
+    idx[9, 2] = idx[9, 1]                                # an expert repeated within a token
     R = moe.moe_rows_capacity(cfg)
     counts = torch.empty(w.n_experts, dtype=torch.int32, device="cuda")
     offsets = torch.empty(w.n_experts + 1, dtype=torch.int32, device="cuda")
@@ -48,6 +51,15 @@ def test_out_of_range_ids_are_skipped_and_flagged():
     moe.moe_permute(cfg, idx, dev["x"], counts, offsets, dest, src, xp, ws)
     assert moe.moe_get_device_error(ws) == moe.MOE_ERR_DEVICE_INDEX
     assert dest[5, 3].item() == -1 and dest[7, 0].item() == -1
+    d = dest.cpu().numpy()
+    assert sorted([d[9, 1], d[9, 2]])[0] == -1 and max(d[9, 1], d[9, 2]) >= 0   # one of the two slots kept
+    bad = d < 0
+    assert bad.sum() == 3 and bad[5, 3] and bad[7, 0]
+    assert (d[~bad] >= 0).all() and int(offsets[-1].item()) == w.T * w.top_k - 3
+    rows = torch.from_numpy(d[~bad].astype(np.int64)).cuda()
+    toks = torch.from_numpy(np.nonzero(~bad)[0].astype(np.int64)).cuda()
+    assert torch.equal(src[rows].long(), toks)                          # each kept row names its token
+    assert torch.equal(xp[rows], dev["x"][toks])                        # and holds its x row
 
 
 def test_corrupt_offsets_are_rejected_on_device():
