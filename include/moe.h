@@ -62,7 +62,8 @@ typedef enum { MOE_SOFTMAX = 0, MOE_SIGMOID = 1 } moe_score_t;
 
 /*
  * Layer shape and policy.
- *   T               tokens in the batch (1 .. 1048576)
+ *   T               tokens in the batch (1 .. 1048576; an empty batch is MOE_ERR_INVALID_ARG: there
+ *                   is nothing to enqueue, so a caller skips the call)
  *   d_model         hidden size d;   bf16: multiple of 128;  f32: multiple of 4
  *   n_experts       routed experts E (1 .. 256)
  *   top_k           experts per token k (1 .. min(E, 8))
