@@ -35,6 +35,22 @@
  *   - R = moe_rows_capacity(cfg) = min(T*k, E*cap) rows hold the kept
  *     (token, expert) pairs grouped by expert; the shared expert's T rows
  *     follow at rows R .. R+T-1 of the grouped outputs.
+ *
+ * Environment switches (each selects among kernel paths that compute the same layer; the
+ * defaults are the paths measured fastest on a B300):
+ *   MOE_FUSED_MLP=0|1    the bf16 expert MLP as one persistent launch of both contractions
+ *                        (default: batches of at most 128 tokens) or two launches; for W8A8
+ *                        layers, =1 selects the one-launch kernel (default: three launches).
+ *                        Same bits either way. Read at every call.
+ *   MOE_MLP_COMBINE=1    with the one-launch bf16 MLP, the combine in its down tiles (per-token
+ *                        counts, the last arrival sums the rows in slot order: the separate
+ *                        combine's bits) instead of a combine launch. Default off. Every call.
+ *   MOE_FUSED_COMBINE=1  bf16 layers: the down projection adds its rows into a float32 output
+ *                        accumulator (red.global.add), then one rounding pass, instead of the
+ *                        combine kernel; the order of the float32 additions depends on
+ *                        scheduling, so the output is not bit-reproducible. Default off. Every call.
+ *   MOE_GEMM_PAIRS=1     the bf16 grouped GEMMs as 2-SM (cta_group::2) pair kernels with 256-row
+ *                        tiles. Default off. Read once per process.
  */
 #ifndef MOE_H
 #define MOE_H
