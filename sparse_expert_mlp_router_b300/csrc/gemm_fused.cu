@@ -183,7 +183,7 @@ grouped_mlp_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_stop = abort_flag + 1;       // COMBINE: the epilogue's snapshot of the abort flag
-  int* s_ncomb = const_cast<int*>(abort_flag + 2);   // COMBINE: tokens the current down tile completed
+  int32_t* s_ncomb = reinterpret_cast<int32_t*>(tmem_holder + 4);   // COMBINE: tokens the down tile completed
   int32_t* s_list = reinterpret_cast<int32_t*>(smem + kListOff);
   int32_t* s_tile_start = reinterpret_cast<int32_t*>(smem + (size_t)kStages * kStageBytes + 256);
   int32_t* s_a_row = s_tile_start + (args.G + 1);
