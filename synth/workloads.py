@@ -64,6 +64,10 @@ WORKLOADS = {
                  description="DeepSeek-V3-shaped layer, 256 routed + 1 shared, sigmoid top-8, capacity 1.25, Zipf(1.2)"),
         Workload("decode_qwen3", T=32, d_model=2048, n_experts=128, top_k=8, d_ff=768,
                  description="decode-shaped batch of 32 tokens on the Qwen3-shaped layer"),
+        # beyond the five: decode on the DeepSeek-V3-shaped layer (dropless, as decode runs)
+        Workload("decode_deepseek", T=32, d_model=7168, n_experts=256, top_k=8, d_ff=2048, n_shared=1,
+                 score="sigmoid", bias_s=1.2,
+                 description="decode-shaped batch of 32 tokens on the DeepSeek-V3-shaped layer, dropless"),
         # reduced sizes for full element-by-element parity against the oracle
         Workload("mini_mixtral", T=300, d_model=256, n_experts=8, top_k=2, d_ff=384, bias_s=1.0),
         Workload("mini_qwen3", T=333, d_model=512, n_experts=32, top_k=8, d_ff=256),
@@ -77,4 +81,5 @@ WORKLOADS = {
 }
 
 FULL = ["tiny_f32", "mixtral_8x7b", "qwen3_30b_a3b", "deepseek_v3", "decode_qwen3"]
+FULL_EXTRA = ["decode_deepseek"]          # full-size parity cases beyond the five benchmarked layers
 MINI = ["tiny_f32", "mini_mixtral", "mini_qwen3", "mini_deepseek", "mini_decode"]

@@ -138,7 +138,7 @@ def _sample_tokens(w, idx, dest_row, n=32):
     return np.array(sorted(toks), dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", synth.workloads.FULL)
+@pytest.mark.parametrize("name", synth.workloads.FULL + synth.workloads.FULL_EXTRA)
 def test_layer_full_size_sampled(name):
     w = synth.WORKLOADS[name]
     cfg = cfg_of(w)

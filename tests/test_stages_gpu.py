@@ -65,7 +65,7 @@ def _check_router(w, x64=None, wr64=None, bias=None, dev=None):
         assert np.abs(gate.sum(axis=1) - 1.0).max() <= 1e-5
 
 
-@pytest.mark.parametrize("name", synth.workloads.FULL)
+@pytest.mark.parametrize("name", synth.workloads.FULL + synth.workloads.FULL_EXTRA)
 def test_router_full_size(name):
     # the five model-shaped routers on their full batches: scores and gates of every token
     w = synth.WORKLOADS[name]
