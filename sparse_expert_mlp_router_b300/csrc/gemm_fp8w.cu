@@ -112,6 +112,13 @@ __device__ __forceinline__ uint32_t widen2(uint32_t pair) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// A 128-row tile (not a resident-token tile) whose group has at most 64 rows left: M=64 MMAs,
+// half the tensor work; its accumulator rows 16 q .. 16 q + 15 sit in TMEM lanes 32 q .. 32 q + 15.
+template <bool RES>
+__device__ __forceinline__ bool half_tile(int rows, int m) {
+  return !RES && rows - m * kBM <= 64;
+}
+
 template <int MODE, bool RES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -307,12 +314,17 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // resident-token tiles hold at most 8 rows: an M=64 MMA (rows 0-15 in TMEM lanes 0-15)
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(RES ? 64 : kBM, 256);
+      // resident-token tiles hold at most 8 rows: an M=64 MMA (rows 0-15 in TMEM lanes 0-15);
+      // a 128-row tile whose group has at most 64 rows left runs M=64 MMAs too (half_tile)
+      constexpr uint32_t idesc128 = ptx::idesc_bf16_f32(RES ? 64 : kBM, 256);
+      constexpr uint32_t idesc64 = ptx::idesc_bf16_f32(64, 256);
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int L = blockIdx.x; L < total_tiles && ok; L += gridDim.x, ++it) {
+        int g, m, n;
+        decode_tile(L, s_tile_start, args.G, args.n_tiles, g, m, n);
+        const uint32_t idesc = half_tile<RES>(s_rows[g], m) ? idesc64 : idesc128;
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!ptx::mbar_wait_bounded(ptx::smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -387,8 +399,11 @@ grouped_gemm_fp8w_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
       epi_bar();
       if (*s_stop != 0) break;
       ptx::tc_fence_after();
-      const bool valid = r_local < C::kRows && (m * C::kRows + r_local) < s_rows[g];
-      const int64_t out_row = (int64_t)s_out_row[g] + m * C::kRows + r_local;
+      // an M=64 tile's row 16 q + i sits in lane i of quarter q (i < 16)
+      const bool m64 = half_tile<RES>(s_rows[g], m);
+      const int r_row = m64 ? (lane < 16 ? quarter * 16 + lane : C::kRows) : r_local;
+      const bool valid = r_row < C::kRows && (m * C::kRows + r_row) < s_rows[g];
+      const int64_t out_row = (int64_t)s_out_row[g] + m * C::kRows + r_row;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * 256);
       if (MODE == 0) {
         __nv_bfloat16* orow = args.out + out_row * args.ldo + (int64_t)n * 128;
